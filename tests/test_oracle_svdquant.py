@@ -1,0 +1,148 @@
+"""Pins for the oracle's SVDQuant pipeline (CPU only).
+
+The pages print no worked example, so the oracle is pinned by what the method
+and the mathematics fix: the smoothing identity, Eckart-Young, the full-rank and
+zero-rank special cases, a pure-Python loop evaluation of the forward on a tiny
+problem, and the method's claim that the low-rank branch makes 4-bit
+quantisation more accurate on outlier-heavy inputs.
+"""
+import numpy as np
+import pytest
+
+from oracle import nvfp4
+from oracle import svdquant as sq
+from w4a4_rank_corrected_e2m1_b300 import synthetic
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    w = synthetic.TINY
+    d = synthetic.make(w)
+    return w, d
+
+
+def test_bf16_rounding_matches_torch():
+    """float64 -> bf16 with one rounding: torch on float32-exact inputs (where its
+    float32 intermediate is exact), and nearest-neighbour brute force on float64 inputs."""
+    import torch
+    rng = np.random.default_rng(4)
+    a = (rng.standard_normal(100000) * np.exp2(rng.uniform(-30, 30, 100000)))
+    a32 = a.astype(np.float32).astype(np.float64)
+    ours = sq.f64_to_bf16(a32)
+    theirs = torch.from_numpy(a32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, theirs)
+    b = sq.f64_to_bf16(a)
+    v = sq.bf16_to_f64(b)
+    up = sq.bf16_to_f64(b + np.uint16(1))        # neighbours in magnitude on the bf16 grid
+    dn = sq.bf16_to_f64(b - np.uint16(1))
+    assert np.all(np.abs(a - v) <= np.abs(a - up)) and np.all(np.abs(a - v) <= np.abs(a - dn))
+
+
+def test_smoothing_identity(tiny):
+    w, d = tiny
+    lam, inv = sq.smoothing_factors(d["X"], d["W"])
+    Xh = sq.smooth_act(d["X"], inv).astype(np.float64)
+    Wh = sq.smooth_weight(d["W"], lam)
+    ref = sq.bf16_to_f64(d["X"]) @ sq.bf16_to_f64(d["W"]).T
+    # x^ carries one fp32 rounding and inv_lambda is fl32(1/lambda): error ~ 2^-23
+    assert sq.rel_fro(Xh @ Wh.T, ref) < 1e-6
+    # outlier channels get the largest lambda (outliers move into the weights)
+    top = np.argsort(lam)[-len(d["outlier_channels"]):]
+    assert set(top) == set(d["outlier_channels"])
+    # lambda follows its closed form on one channel, computed by hand
+    c = int(d["outlier_channels"][0])
+    xm = np.max(np.abs(sq.bf16_to_f64(d["X"][:, c])))
+    wm = np.max(np.abs(sq.bf16_to_f64(d["W"][:, c])))
+    assert lam[c] == np.float32(np.sqrt(xm / wm))
+
+
+def test_eckart_young(tiny):
+    w, d = tiny
+    lam, _ = sq.smoothing_factors(d["X"], d["W"])
+    Wh = sq.smooth_weight(d["W"], lam)
+    for r in (0, 4, 16, 64):
+        L1, L2, _ = sq.lowrank_factors(Wh, r)
+        res = np.sum((Wh.T - L1 @ L2) ** 2)
+        ev = np.sort(np.linalg.eigvalsh(Wh.T @ Wh))[::-1]       # sigma^2, independent route
+        tail = np.sum(np.clip(ev[r:], 0, None))
+        assert abs(res - tail) <= 1e-9 * np.sum(ev)
+        if r:
+            assert np.allclose(L1.T @ L1, np.eye(r), atol=1e-12)   # L1 orthonormal
+
+
+def test_full_rank_leaves_zero_residual(tiny):
+    w, d = tiny
+    lam, inv = sq.smoothing_factors(d["X"], d["W"])
+    Wh = sq.smooth_weight(d["W"], lam)
+    L1, L2, _ = sq.lowrank_factors(Wh, w.K)
+    assert np.linalg.norm(Wh - (L1 @ L2).T) <= 1e-12 * np.linalg.norm(Wh)
+    p = sq.pack(d["W"], d["bias"], w.K, Xcal_bits=d["X"])
+    # only the bf16 rounding of the factors is left in R
+    assert np.linalg.norm(p["R"]) < 2 ** -7 * np.linalg.norm(Wh)
+    Y = sq.forward(d["X"], p)
+    ref = sq.exact_product(d["X"], d["W"], d["bias"])
+    assert sq.rel_fro(Y, ref) < 2e-3
+
+
+def test_unsmoothed_rank0_is_plain_w4a4(tiny):
+    w, d = tiny
+    p = sq.pack(d["W"], d["bias"], 0, Xcal_bits=None, smooth=False)
+    wf = sq.bf16_to_f32(d["W"])
+    cw, sw = nvfp4.quantize_blocks(wf, nvfp4.global_scale(np.max(np.abs(wf))))
+    assert np.array_equal(p["R_codes"], cw) and np.array_equal(p["R_scales"], sw)
+    assert np.array_equal(p["R"], wf)
+    x = sq.bf16_to_f32(d["X"])
+    p["s_gX"] = nvfp4.global_scale(np.max(np.abs(x)))
+    cx, sx, _ = sq.quantize_act(d["X"], p["inv_lambda"], p["s_gX"])
+    cx2, sx2 = nvfp4.quantize_blocks(x, p["s_gX"])
+    assert np.array_equal(cx, cx2) and np.array_equal(sx, sx2)
+    assert np.allclose(sq.forward(d["X"], p), sq.naive_w4a4(d["X"], d["W"], d["bias"]), rtol=0, atol=1e-12)
+
+
+def test_forward_against_python_loops():
+    """4 x 16 x 16 (and 3 x 32 x 5): the forward written as explicit scalar loops."""
+    for (M, K, N, r) in [(4, 16, 16, 4), (3, 32, 5, 2)]:
+        w = synthetic.scaled(synthetic.TINY, M=M, K=K, N=N, rank=r, n_outlier=1, spike_rank=1)
+        d = synthetic.make(w, seed=7)
+        p = sq.pack(d["W"], d["bias"], r, Xcal_bits=d["X"])
+        Y = sq.forward(d["X"], p)
+        cx, sx, xh = sq.quantize_act(d["X"], p["inv_lambda"], p["s_gX"])
+        L1 = sq.bf16_to_f64(p["L1"])
+        L2 = sq.bf16_to_f64(p["L2"])
+        b = sq.bf16_to_f64(p["bias"])
+        a = float(np.float32(p["s_gX"]) * np.float32(p["s_gW"]))
+        for m in range(M):
+            for n in range(N):
+                acc = 0.0
+                for k in range(K):
+                    xv = float(nvfp4.e2m1_decode(cx[m, k])) * float(nvfp4.e4m3_decode(sx[m, k // 16]))
+                    wv = float(nvfp4.e2m1_decode(p["R_codes"][n, k])) * float(nvfp4.e4m3_decode(p["R_scales"][n, k // 16]))
+                    acc += xv * wv
+                lr = 0.0
+                for j in range(r):
+                    t = 0.0
+                    for k in range(K):
+                        t += float(xh[m, k]) * L1[k, j]
+                    lr += t * L2[j, n]
+                assert abs(a * acc + lr + b[n] - Y[m, n]) <= 1e-9 * (1 + abs(Y[m, n]))
+
+
+@pytest.mark.parametrize("name", ["tiny", "qkv_small"])
+def test_svdquant_beats_naive_w4a4_on_outliers(name):
+    w = {c.name: c for c in synthetic.parity_cases()}[name]
+    d = synthetic.make(w)
+    ref = sq.exact_product(d["X"], d["W"], d["bias"])
+    p = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"])
+    e_svdq = sq.rel_fro(sq.forward(d["X"], p), ref)
+    e_naive = sq.rel_fro(sq.naive_w4a4(d["X"], d["W"], d["bias"]), ref)
+    assert e_svdq < e_naive, (e_svdq, e_naive)
+
+
+def test_residual_against_rounded_factors(tiny):
+    w, d = tiny
+    p = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"])
+    Wh = sq.smooth_weight(d["W"], p["lam"])
+    LL = sq.bf16_to_f64(p["L1"]) @ sq.bf16_to_f64(p["L2"])
+    assert np.array_equal(p["R"], (Wh - LL.T).astype(np.float32))
+    # the rank-r branch carries the spike: the residual is much smaller than W^
+    assert np.linalg.norm(p["R"]) < 0.8 * np.linalg.norm(Wh)
