@@ -1,0 +1,311 @@
+"""Benchmark of the SVDQuant W4A4 linear layer (svdq_linear_forward) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload flux_mlp_up] [--impl reference]
+
+One step = one pass of the whole hot path (kernel 1: smoothing + NVFP4 quantisation +
+down-projection; kernel 2: block-scaled FP4 tensor-core GEMM + up-projection + bias) over
+one batch of synthetic FLUX-shaped activations already resident in HBM.  L2 is flushed
+(256 MiB write) before every timed step, outside the timed events.  Prints one JSON line.
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU with its own batch
+(the layer shards over tokens with no exchange): weak scaling, time = max over ranks.
+
+--impl reference times the CPU oracle (the plain numpy restatement of the method) on the
+host cores, on a bounded sample of rows of the same workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from w4a4_rank_corrected_e2m1_b300 import synthetic  # noqa: E402
+
+METRIC = "fused SVDQuant W4A4 linear TFLOPS & tokens/s at FLUX shapes; % of FP4 roofline"
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on B300
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="flux_mlp_up", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+def workload_flops(w, rows=None):
+    M = w.M if rows is None else rows
+    return 2.0 * M * w.N * w.K + 2.0 * M * w.K * w.rank + 2.0 * M * w.rank * w.N
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample(w, d, budget_s=12.0, max_rows=None):
+    """Time the oracle forward on a bounded sample of rows; returns (TFLOP/s, rows, seconds, threads)."""
+    from threadpoolctl import threadpool_info
+    from oracle import svdquant as sq
+    p = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"][: min(w.M, 1024)])
+    rows = 16
+    best = None
+    while True:
+        t0 = time.perf_counter()
+        sq.forward(d["X"][:rows], p)
+        dt = time.perf_counter() - t0
+        best = (rows, dt)
+        if dt > budget_s / 4 or rows >= w.M or (max_rows and rows >= max_rows):
+            break
+        rows = min(w.M, rows * 4)
+    rows, dt = best
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    return workload_flops(w, rows) / dt / 1e12, rows, dt, threads
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    d = synthetic.make(w)
+    from threadpoolctl import threadpool_info
+    from oracle import svdquant as sq
+    p = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"][: min(w.M, 1024)])
+    rows = min(w.M, 128)
+    for _ in range(args.warmup):
+        sq.forward(d["X"][:rows], p)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        sq.forward(d["X"][:rows], p)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    val = workload_flops(w, rows) * args.steps / tot / 1e12
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    sample = f"{rows} of {w.M} token rows per step (oracle forward, weights pre-packed)"
+    out = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "rank": w.rank},
+        "tokens_per_s": rows * args.steps / tot,
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+                         "threads": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+        if self.p is None:
+            return out
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return out
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        out.update(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                   reasons=reasons, samples=len(rows))
+        return out
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from w4a4_rank_corrected_e2m1_b300 import svdq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    d = synthetic.make(w)
+    M, K, N = w.M, w.K, w.N
+    t_pack = time.perf_counter()
+    layer = svdq.Layer(d["W"], w.rank, bias=d["bias"], Xcal=d["X"], M_max=M, device=local)
+    t_pack = time.perf_counter() - t_pack
+    layer0 = svdq.Layer(d["W"], 0, bias=d["bias"], Xcal=d["X"], M_max=M, device=local)
+    stream = torch.cuda.current_stream()
+
+    # distinct activation batches per step (rank-specific seeds), resident in HBM
+    nbuf = 4
+    Xs = [torch.from_numpy(synthetic.make_x(w, M, seed=1000 * rank + i).view(np.int16)).cuda() for i in range(nbuf)]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def timed_loop(fn, steps, warm):
+        for i in range(warm):
+            fn(i)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn(i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    clocks = Clocks(torch.cuda.current_device())
+    fwd_ms = timed_loop(lambda i: layer.forward(Xs[i % nbuf], Y, M, stream), args.steps, args.warmup)
+    clk = clocks.stop()
+    layer.check_error()
+
+    # per-kernel times through the same kernels called one at a time
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(svdq.scales_bytes(M, K), dtype=torch.uint8, device="cuda")
+    T = torch.empty((M, max(layer.info.r_pad, 8)), dtype=torch.int16, device="cuda")
+    k_ev = []
+
+    def split_step(i):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        layer.quantize_act(Xs[i % nbuf], M, codes, scales, T, stream)
+        e1.record(stream)
+        layer.gemm_quantized(codes, scales, T, Y, M, stream)
+        e2.record(stream)
+        k_ev.append((e0, e1, e2))
+
+    timed_loop(split_step, args.steps, args.warmup)
+    k_ev = k_ev[args.warmup:]
+    t_k1 = statistics.median(a.elapsed_time(b) for a, b, _ in k_ev)
+    t_k2 = statistics.median(b.elapsed_time(c) for _, b, c in k_ev)
+    layer.check_error()
+
+    # the same layer with the low-rank branch removed (rank 0): the branch's added time
+    r0_ms = timed_loop(lambda i: layer0.forward(Xs[i % nbuf], Y, M, stream), args.steps, args.warmup)
+
+    # end to end through the host-buffer entry point: pinned X in, Y out, copies timed
+    layer.reserve(M, host_staging=True)
+    Xh = torch.from_numpy(synthetic.make_x(w, M, seed=77 + rank).view(np.int16)).pin_memory()
+    Yh = torch.empty((M, N), dtype=torch.int16).pin_memory()
+    for _ in range(max(1, args.warmup // 2)):
+        layer.forward_host(Xh, Yh, M, stream)
+    barrier()
+    e2e_t = []
+    for _ in range(max(3, args.steps // 2)):
+        t0 = time.perf_counter()
+        layer.forward_host(Xh, Yh, M, stream)
+        e2e_t.append(time.perf_counter() - t0)
+    barrier()
+
+    # max over ranks
+    ms_step = sum(fwd_ms) / len(fwd_ms)
+    if world > 1:
+        tt = torch.tensor([ms_step, statistics.median(e2e_t)], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step, e2e_med = float(tt[0]), float(tt[1])
+    else:
+        e2e_med = statistics.median(e2e_t)
+
+    if rank == 0:
+        hbm, bf16, src = peaks()
+        fp4_peak = bf16 * FP4_OVER_BF16
+        flops = workload_flops(w)
+        tflops = flops * world / (ms_step * 1e-3) / 1e12
+        k2_fp4_flops = 2.0 * M * N * K
+        k2_achieved = k2_fp4_flops / (t_k2 * 1e-3) / 1e12
+        k1_bytes = M * K * 2 + M * K // 2 + M * K // 16 + M * w.rank * 2 + K * w.rank * 2 + K * 4
+        r0_step = sum(r0_ms) / len(r0_ms)
+        out = {
+            "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4(e2m1,e4m3)+bf16, f32 accumulate", "data": "synthetic",
+            "config": {"workload": w.name, "M": M, "K": K, "N": N, "rank": w.rank, "per_gpu_tokens": M,
+                       "l2": "flushed before every timed step (256 MiB write outside the timed events)",
+                       "parallelism": f"replicas x{world} (token shards, no collective)"},
+            "tokens_per_s": M * world / (ms_step * 1e-3),
+            "kernels_ms": {"k1_actquant": t_k1, "k2_fp4gemm": t_k2},
+            "roofline": {"bound": "tensor", "kernel": "k2_fp4gemm", "achieved": k2_achieved, "peak": fp4_peak,
+                         "unit": "TFLOP/s", "frac": k2_achieved / fp4_peak, "traffic": None,
+                         "peak_source": f"{src} bf16 {bf16} TFLOP/s x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
+            "roofline_k1": {"bound": "hbm", "kernel": "k1_actquant", "achieved": k1_bytes / (t_k1 * 1e-3) / 1e9,
+                            "peak": hbm, "unit": "GB/s", "frac": k1_bytes / (t_k1 * 1e-3) / 1e9 / hbm,
+                            "traffic": None},
+            "lowrank": {"rank": w.rank, "fwd_ms": ms_step, "fwd_rank0_ms": r0_step,
+                        "added_frac_of_4bit_gemm": (ms_step - r0_step) / t_k2},
+            "e2e": {"value": flops * world / e2e_med / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
+                    "ms_per_step": e2e_med * 1e3},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk,
+            "pack_s": t_pack,
+        }
+        if not args.no_cpu_baseline:
+            v, rows, dt, threads = oracle_sample(w, d)
+            out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+                                   "threads": threads, "kind": "oracle",
+                                   "sample": f"oracle forward on {rows} of {M} token rows, {dt:.2f} s"}
+        print(json.dumps(out), flush=True)
+    layer.close()
+    layer0.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = synthetic.get(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,214 @@
+/*
+ * svdq.h -- C ABI of the SVDQuant W4A4 (NVFP4 / E2M1) linear layer for B300 (sm_103a).
+ *
+ * The layer (SVDQuant, as the Nunchaku engine runs it; "What SVDQuant actually
+ * does" and "How Nunchaku four bit quantization actually works" sections of the
+ * aiflownews article on Nunchaku in Diffusers):
+ *
+ *     Y = alpha * Q4(X diag(lambda)^-1) Q4(R)^T  +  ((X diag(lambda)^-1) L1) L2  +  b
+ *
+ *   lambda  per-channel smoothing factors that move activation outliers into
+ *           the weights (stage one of the method),
+ *   L1 L2   the rank-r 16-bit (bfloat16) SVD branch of the smoothed weight
+ *           (stage two),
+ *   R       the 4-bit residual W diag(lambda) - (L1 L2)^T (stage three),
+ *   Q4      NVFP4: E2M1 codes, one E4M3 scale per 16 elements along K,
+ *           rounding to nearest even, saturating,
+ *   alpha   s_gX * s_gW, the two float32 per-tensor global scales.
+ *
+ * Conventions (every call):
+ *   - Matrices are row-major.  X is M x K, W is N x K (a linear layer's weight),
+ *     Y is M x N.  bfloat16 values are passed as their uint16 bit patterns.
+ *   - "host" pointers are ordinary CPU memory; "device" pointers are CUDA
+ *     global memory on the handle's device.  The caller owns every buffer it
+ *     passes; the library never frees caller memory and keeps no pointer to it
+ *     after the call returns (except set_workspace, which borrows until reset).
+ *   - Every call returns svdq_status_t; no C++ exception crosses the ABI.
+ *     svdq_last_error() gives a message for the calling thread's last failure.
+ *   - Calls taking a stream are asynchronous on that stream (cudaStream_t
+ *     passed as void*, NULL = legacy default stream).  They do not allocate
+ *     and do not synchronise.  Kernel launch errors are reported as
+ *     SVDQ_ERR_CUDA; a kernel that gave up on a bounded wait records
+ *     SVDQ_ERR_TIMEOUT in the handle's device error word (svdq_check_error).
+ *   - Shape rules for the CUDA path: K % 64 == 0, N % 16 == 0, 0 <= rank <= 128,
+ *     rank % 16 == 0, rank <= min(N, K), M >= 0 (any M; M = 0 is a no-op).
+ *   - The device must be compute capability 10.3 (B300); anything else gives
+ *     SVDQ_ERR_ARCH before any launch.
+ *
+ * Device layouts (what svdq_quantize_act writes; documented so that callers
+ * and tests can read it):
+ *   x_codes   M x K/2 bytes, row-major; element k of a row sits in byte k/2,
+ *             low nibble for even k, high nibble for odd k; nibble = E2M1 code
+ *             (bit 3 sign, bits 0..2 magnitude index into {0,.5,1,1.5,2,3,4,6}).
+ *   x_scales  E4M3 bytes in 128 x 4 tiles, the tensor-core scale layout: with
+ *             KG = 4 * ceil(K / 256) groups of 64 columns per row block,
+ *             the scale of row m, 16-column block j lives at byte
+ *               ((m / 128) * KG + j / 4) * 512 + (m % 32) * 16 + ((m % 128) / 32) * 4 + (j % 4).
+ *             Rows are padded to a multiple of 128 (padding rows hold 0).
+ *             Size: svdq_scales_bytes(M, K).
+ *   T         M x r_pad bfloat16, r_pad = 64 * ceil(rank / 64) (0 if rank == 0),
+ *             T[m][j] = round_bf16( (X^ L1)[m][j] / alpha ) for j < rank, 0 beyond.
+ *             The 1/alpha folding lets the tensor-core epilogue add the
+ *             low-rank product into the same accumulator as the 4-bit product.
+ */
+#ifndef SVDQ_H_
+#define SVDQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct svdq_layer* svdq_handle_t; /* opaque; owns all device copies of the packed layer */
+
+typedef enum {
+  SVDQ_OK = 0,
+  SVDQ_ERR_INVALID_ARG = 1,      /* null pointer, negative size, bad flag      */
+  SVDQ_ERR_UNSUPPORTED_SHAPE = 2,/* violates the shape rules above             */
+  SVDQ_ERR_ARCH = 3,             /* device is not compute capability 10.3      */
+  SVDQ_ERR_OOM = 4,              /* host or device allocation failed           */
+  SVDQ_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed       */
+  SVDQ_ERR_TIMEOUT = 6,          /* a kernel gave up a bounded wait            */
+  SVDQ_ERR_WORKSPACE = 7         /* no workspace, or too small for this M      */
+} svdq_status_t;
+
+#define SVDQ_NO_SMOOTH 1u /* lambda = 1: skip smoothing                         */
+
+/* Parameters of the offline packing step. */
+typedef struct {
+  int64_t N, K, rank;
+  const uint16_t* W_bf16;     /* host, N x K, required                                    */
+  const uint16_t* bias_bf16;  /* host, N, NULL = zero bias                                */
+  const uint16_t* Xcal_bf16;  /* host, Mcal x K calibration activations, NULL = none      */
+  int64_t Mcal;
+  const float* lambda;        /* host, K; overrides Xcal for lambda when non-NULL         */
+  float s_gX;                 /* activation global scale when Xcal is NULL (0 -> 1.0)     */
+  const uint16_t* L1_bf16;    /* host, K x rank; with L2 replaces the SVD (NULL = SVD)    */
+  const uint16_t* L2_bf16;    /* host, rank x N                                           */
+  uint32_t flags;             /* SVDQ_NO_SMOOTH                                           */
+  int32_t svd_power_iters;    /* randomized SVD subspace iterations (<= 0 -> 6)           */
+  int32_t svd_oversample;     /* extra sketch columns (<= 0 -> 16)                        */
+  uint64_t svd_seed;          /* sketch seed                                              */
+  int64_t M_max;              /* reserve a library-owned workspace for M <= M_max (0 = none) */
+  int32_t device;             /* CUDA device ordinal for the packed layer                */
+  void* stream;               /* cudaStream_t used for the upload                         */
+} svdq_pack_params_t;
+
+/* The packed layer in canonical host layouts (caller-allocated buffers). */
+typedef struct {
+  float* lambda;        /* K                                                   */
+  float* inv_lambda;    /* K, fl32(1 / lambda)                                 */
+  uint16_t* L1_bf16;    /* K x rank                                            */
+  uint16_t* L2_bf16;    /* rank x N                                            */
+  uint8_t* R_codes;     /* N x K/2, same nibble order as x_codes               */
+  uint8_t* R_scales;    /* N x K/16 E4M3, row-major (not tiled)                */
+  uint16_t* bias_bf16;  /* N                                                   */
+  float s_gW, s_gX, alpha;
+} svdq_packed_host_t;
+
+typedef struct {
+  int64_t N, K, rank, r_pad, M_max;
+  float s_gW, s_gX, alpha;
+  int32_t device, sm_count;
+} svdq_info_t;
+
+/*
+ * svdq_pack_host -- the offline step alone, on the CPU (no CUDA call).
+ * Smoothing lambda_c = sqrt(max|X_c| / max|W_c|) (stage one), top-rank SVD of
+ * (W diag(lambda))^T by randomized subspace iteration with Sigma on L2 (stage
+ * two), R = W diag(lambda) - (L1 L2)^T against the bf16 factors, NVFP4
+ * quantisation of R with s_gW = amax|R| / 2688 (stage three).  All outputs go
+ * to caller buffers in `out`.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, OOM.
+ */
+svdq_status_t svdq_pack_host(const svdq_pack_params_t* p, svdq_packed_host_t* out);
+
+/*
+ * svdq_pack_weights -- svdq_pack_host, then the device layouts, uploaded to
+ * handle-owned device memory on p->device (cudaMalloc + cudaMemcpyAsync on
+ * p->stream, synchronised before return).  *out receives the handle; destroy
+ * it with svdq_destroy.  With p->M_max > 0 a workspace for M <= M_max is
+ * reserved as by svdq_reserve.
+ */
+svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out);
+
+/* Frees every device and host allocation the handle owns.  NULL is a no-op. */
+svdq_status_t svdq_destroy(svdq_handle_t h);
+
+svdq_status_t svdq_get_info(svdq_handle_t h, svdq_info_t* info);
+
+/* Copy of the packed layer in canonical host layouts (see svdq_packed_host_t). */
+svdq_status_t svdq_export(svdq_handle_t h, svdq_packed_host_t* out);
+
+/* Bytes of the activation-scale buffer for M rows (tiled layout above). */
+int64_t svdq_scales_bytes(int64_t M, int64_t K);
+
+/*
+ * Workspace: the forward keeps the quantised activations, T and the split-K
+ * partial sums of the down-projection in a device workspace.
+ * svdq_workspace_size gives the bytes needed for M rows; svdq_reserve makes the
+ * handle allocate (cudaMalloc) and own one for M <= M_max; svdq_set_workspace
+ * lends caller memory instead (256-byte aligned, NULL to drop it).  With
+ * host_staging != 0 the size also covers the device copies of X and Y used by
+ * svdq_linear_forward_host.  Concurrent calls on one handle share the
+ * workspace and must be ordered on one stream.
+ */
+svdq_status_t svdq_workspace_size(svdq_handle_t h, int64_t M, int32_t host_staging, size_t* bytes);
+svdq_status_t svdq_reserve(svdq_handle_t h, int64_t M_max, int32_t host_staging);
+svdq_status_t svdq_set_workspace(svdq_handle_t h, void* dev_ptr, size_t bytes, int64_t M_max,
+                                 int32_t host_staging);
+
+/*
+ * svdq_quantize_act -- kernel 1 alone: x^ = fl32(x * inv_lambda), NVFP4 codes
+ * and E4M3 block scales of x^ (block quantiser with s_gX, bit-exact with the
+ * format rules above) and T = X^ L1 / alpha (low-rank down-projection of stage
+ * two, float32 accumulation, bfloat16 out).  X: device M x K bf16.  x_codes,
+ * x_scales, T: device buffers in the layouts above (T may be NULL when
+ * rank == 0).  Uses the handle's workspace for split-K partials.
+ */
+svdq_status_t svdq_quantize_act(svdq_handle_t h, const void* X_bf16, int64_t M, void* x_codes,
+                                void* x_scales, void* T_bf16, void* stream);
+
+/*
+ * svdq_gemm_quantized -- kernel 2 alone on already-quantised activations:
+ * Y = alpha * (acc_fp4 + T L2) + b with the block-scaled FP4 tensor-core GEMM
+ * (the "dominant 4 bit path") and the low-rank up-projection added into the
+ * same accumulator.  Inputs in the layouts above; Y: device M x N bf16, fully
+ * overwritten, written once.
+ */
+svdq_status_t svdq_gemm_quantized(svdq_handle_t h, const void* x_codes, const void* x_scales,
+                                  const void* T_bf16, void* Y_bf16, int64_t M, void* stream);
+
+/*
+ * svdq_linear_forward -- the layer: kernel 1 then kernel 2 on `stream`.
+ * X: device M x K bf16 (read once).  Y: device M x N bf16 (written once, must
+ * not alias X).  Needs a workspace for M (svdq_reserve / svdq_set_workspace).
+ */
+svdq_status_t svdq_linear_forward(svdq_handle_t h, const void* X_bf16, void* Y_bf16, int64_t M,
+                                  void* stream);
+
+/*
+ * svdq_linear_forward_host -- the layer on HOST buffers: copies X (host, ideally
+ * pinned) to the workspace's device staging, runs svdq_linear_forward, copies Y
+ * back to host and synchronises the stream.  Needs a workspace reserved with
+ * host_staging != 0.
+ */
+svdq_status_t svdq_linear_forward_host(svdq_handle_t h, const uint16_t* X_host, uint16_t* Y_host,
+                                       int64_t M, void* stream);
+
+/*
+ * svdq_check_error -- synchronises the handle's device, reads and clears the
+ * device error word that the kernels set when a bounded wait gives up.
+ * Returns SVDQ_OK or SVDQ_ERR_TIMEOUT (or SVDQ_ERR_CUDA for a sticky CUDA error).
+ */
+svdq_status_t svdq_check_error(svdq_handle_t h);
+
+const char* svdq_status_string(svdq_status_t s);
+const char* svdq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVDQ_H_ */

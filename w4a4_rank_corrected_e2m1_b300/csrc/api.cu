@@ -1,0 +1,528 @@
+// C-ABI entry points of the SVDQuant W4A4 linear layer (declared in include/svdq.h).
+//
+// The handle owns the packed layer on one device: the tiled NVFP4 residual, the folded and
+// permuted L1 for kernel 1, L2^T for kernel 2, 1/lambda, the bias, a device error word and
+// (optionally) a workspace.  The forward is two launches on the caller's stream: kernel 1
+// (smoothing + NVFP4 quantisation + down-projection, one read of X) and kernel 2 (block-scaled
+// FP4 tensor-core GEMM + up-projection + bias, one write of Y).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "svdq_internal.h"
+
+using namespace svdq;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+svdq_status_t fail(svdq_status_t s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+svdq_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(SVDQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void* dalloc(size_t bytes, cudaError_t* e) {
+  void* p = nullptr;
+  *e = cudaMalloc(&p, bytes ? bytes : 256);
+  return *e == cudaSuccess ? p : nullptr;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+namespace svdq {
+
+bool encode_map_2d(void* map, int dtype_bytes, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle128,
+                   std::string* err) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  const CUtensorMapDataType dt = dtype_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[2] = {inner, outer < 1 ? 1 : outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(reinterpret_cast<CUtensorMap*>(map), dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(int(r));
+    return false;
+  }
+  return true;
+}
+
+}  // namespace svdq
+
+struct svdq_layer {
+  HostPack host;
+  int device = 0;
+  int sm_count = 0;
+  int64_t r_pad = 0;
+  // device copies
+  uint8_t* d_R_codes = nullptr;
+  uint8_t* d_R_scales = nullptr;   // tiled, rows padded to 256
+  uint16_t* d_L2t = nullptr;       // N x r_pad
+  uint16_t* d_Lperm = nullptr;     // folded + permuted L1
+  float* d_inv_lambda = nullptr;
+  uint16_t* d_bias = nullptr;
+  int* d_err = nullptr;
+  K2Maps maps{};                   // B and L2 filled at pack
+  // workspace
+  unsigned char* ws = nullptr;
+  size_t ws_bytes = 0;
+  bool ws_owned = false;
+  int64_t ws_M = 0;
+  bool ws_staging = false;
+  float six_sgX = 6.f, inv_alpha = 1.f;
+};
+
+namespace {
+
+struct WsLayout {
+  size_t codes, scales, T, partial, counters, Xs, Ys, total;
+};
+
+WsLayout ws_layout(const svdq_layer* h, int64_t M, bool staging) {
+  WsLayout w{};
+  const int64_t K = h->host.K, N = h->host.N, r = h->host.rank;
+  size_t off = 0;
+  w.codes = off; off += align256(size_t(M) * K / 2);
+  w.scales = off; off += align256(size_t(svdq_scales_bytes(M, K)));
+  w.T = off; off += align256(size_t(M) * h->r_pad * 2);
+  // split-K partial sums: bounded over every M' <= M by (3 * SMs + row tiles) row tiles
+  const int64_t rows = r > 64 ? 64 : 128;
+  const int64_t tiles = ceil_div(M, rows);
+  w.partial = off; off += align256(r ? size_t(3 * h->sm_count + tiles) * rows * r * sizeof(float) : 0);
+  w.counters = off; off += align256(size_t(tiles + 1) * sizeof(unsigned int));
+  w.Xs = off; off += staging ? align256(size_t(M) * K * 2) : 0;
+  w.Ys = off; off += staging ? align256(size_t(M) * N * 2) : 0;
+  w.total = off;
+  return w;
+}
+
+svdq_status_t check_arch(int device) {
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(SVDQ_ERR_ARCH, "device " + std::to_string(device) + " is sm_" + std::to_string(prop.major) +
+                                   std::to_string(prop.minor) + ", this library is built for sm_103a (B300)");
+  return SVDQ_OK;
+}
+
+svdq_status_t check_shape(int64_t N, int64_t K, int64_t r) {
+  if (K % 64 != 0 || N % 16 != 0 || r < 0 || r > 128 || r % 16 != 0 || r > std::min(N, K))
+    return fail(SVDQ_ERR_UNSUPPORTED_SHAPE,
+                "CUDA path needs K % 64 == 0, N % 16 == 0, rank % 16 == 0, 0 <= rank <= min(128, N, K)");
+  return SVDQ_OK;
+}
+
+void free_layer(svdq_layer* h) {
+  cudaFree(h->d_R_codes);
+  cudaFree(h->d_R_scales);
+  cudaFree(h->d_L2t);
+  cudaFree(h->d_Lperm);
+  cudaFree(h->d_inv_lambda);
+  cudaFree(h->d_bias);
+  cudaFree(h->d_err);
+  if (h->ws_owned) cudaFree(h->ws);
+}
+
+svdq_status_t attach_workspace(svdq_layer* h, void* ptr, size_t bytes, int64_t M_max, bool staging, bool owned,
+                               cudaStream_t stream) {
+  if (h->ws_owned && h->ws) cudaFree(h->ws);
+  h->ws = static_cast<unsigned char*>(ptr);
+  h->ws_bytes = bytes;
+  h->ws_owned = owned;
+  h->ws_M = ptr ? M_max : 0;
+  h->ws_staging = ptr ? staging : false;
+  if (ptr) {
+    const WsLayout w = ws_layout(h, M_max, staging);
+    cudaError_t e = cudaMemsetAsync(h->ws + w.counters, 0, w.Xs - w.counters, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing workspace counters");
+  }
+  return SVDQ_OK;
+}
+
+svdq_status_t launch_k1(svdq_layer* h, const void* X, int64_t M, void* codes, void* scales, void* T,
+                        cudaStream_t stream) {
+  const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
+  K1Args a{};
+  a.X = static_cast<const uint16_t*>(X);
+  a.inv_lambda = h->d_inv_lambda;
+  a.Lperm = h->d_Lperm;
+  a.x_codes = static_cast<uint8_t*>(codes);
+  a.x_scales = static_cast<uint8_t*>(scales);
+  a.T = static_cast<uint16_t*>(T);
+  a.partial = reinterpret_cast<float*>(h->ws + w.partial);
+  a.counters = reinterpret_cast<unsigned int*>(h->ws + w.counters);
+  a.M = M;
+  a.K = h->host.K;
+  a.rank = int(h->host.rank);
+  a.r_pad = int(h->r_pad);
+  a.s_gX = h->host.s_gX;
+  a.six_sgX = h->six_sgX;
+  a.inv_alpha = h->inv_alpha;
+  const K1Plan plan = k1_plan(M, a.K, a.rank, h->sm_count);
+  const int e = k1_launch(a, plan, stream);
+  if (e != 0) return cuda_fail(cudaError_t(e), "kernel 1 launch");
+  return SVDQ_OK;
+}
+
+svdq_status_t launch_k2(svdq_layer* h, const void* codes, const void* scales, const void* T, void* Y, int64_t M,
+                        cudaStream_t stream) {
+  const int64_t K = h->host.K, N = h->host.N;
+  K2Maps maps = h->maps;
+  std::string err;
+  if (!encode_map_2d(maps.A, 1, codes, K / 2, M, K / 2, 128, 128, 1, &err) ||
+      !encode_map_2d(maps.Y, 2, Y, N, M, N * 2, 64, 32, 1, &err))
+    return fail(SVDQ_ERR_CUDA, err);
+  if (h->host.rank > 0 && !encode_map_2d(maps.T, 2, T, h->r_pad, M, h->r_pad * 2, 64, 128, 1, &err))
+    return fail(SVDQ_ERR_CUDA, err);
+  K2Args a{};
+  a.sfa = static_cast<const uint8_t*>(scales);
+  a.sfb = h->d_R_scales;
+  a.bias = h->d_bias;
+  a.err = h->d_err;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.rank = int(h->host.rank);
+  a.alpha = h->host.alpha;
+  const int e = k2_launch(maps, a, h->sm_count, stream);
+  if (e != 0) return cuda_fail(cudaError_t(e), "kernel 2 launch");
+  return SVDQ_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* svdq_status_string(svdq_status_t s) {
+  switch (s) {
+    case SVDQ_OK: return "ok";
+    case SVDQ_ERR_INVALID_ARG: return "invalid argument";
+    case SVDQ_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case SVDQ_ERR_ARCH: return "unsupported device architecture";
+    case SVDQ_ERR_OOM: return "out of memory";
+    case SVDQ_ERR_CUDA: return "CUDA error";
+    case SVDQ_ERR_TIMEOUT: return "kernel wait timed out";
+    case SVDQ_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* svdq_last_error(void) { return g_last_error.c_str(); }
+
+int64_t svdq_scales_bytes(int64_t M, int64_t K) {
+  if (M < 0 || K < 0) return 0;
+  return ceil_div(M, 128) * scale_groups(K) * 512;
+}
+
+svdq_status_t svdq_pack_host(const svdq_pack_params_t* p, svdq_packed_host_t* out) {
+  if (!p || !out) return fail(SVDQ_ERR_INVALID_ARG, "null argument");
+  HostPack hp;
+  std::string err;
+  svdq_status_t s = pack_on_host(p, &hp, &err);
+  if (s != SVDQ_OK) return fail(s, err);
+  const int64_t N = hp.N, K = hp.K, r = hp.rank;
+  if (out->lambda) std::memcpy(out->lambda, hp.lambda.data(), sizeof(float) * K);
+  if (out->inv_lambda) std::memcpy(out->inv_lambda, hp.inv_lambda.data(), sizeof(float) * K);
+  if (out->L1_bf16 && r) std::memcpy(out->L1_bf16, hp.L1.data(), sizeof(uint16_t) * K * r);
+  if (out->L2_bf16 && r) std::memcpy(out->L2_bf16, hp.L2.data(), sizeof(uint16_t) * r * N);
+  if (out->R_codes) std::memcpy(out->R_codes, hp.R_codes.data(), hp.R_codes.size());
+  if (out->R_scales) std::memcpy(out->R_scales, hp.R_scales.data(), hp.R_scales.size());
+  if (out->bias_bf16) std::memcpy(out->bias_bf16, hp.bias.data(), sizeof(uint16_t) * N);
+  out->s_gW = hp.s_gW;
+  out->s_gX = hp.s_gX;
+  out->alpha = hp.alpha;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out) {
+  if (!p || !out) return fail(SVDQ_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  svdq_status_t s = check_shape(p->N, p->K, p->rank);
+  if (s != SVDQ_OK) return s;
+  if (p->M_max < 0) return fail(SVDQ_ERR_INVALID_ARG, "M_max must be >= 0");
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (p->device < 0 || p->device >= ndev) return fail(SVDQ_ERR_INVALID_ARG, "no such device");
+  s = check_arch(p->device);
+  if (s != SVDQ_OK) return s;
+
+  svdq_layer* h = new (std::nothrow) svdq_layer();
+  if (!h) return fail(SVDQ_ERR_OOM, "host allocation failed");
+  std::string err;
+  s = pack_on_host(p, &h->host, &err);
+  if (s != SVDQ_OK) {
+    delete h;
+    return fail(s, err);
+  }
+  DeviceGuard guard(p->device);
+  cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+  h->device = p->device;
+  cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, p->device);
+  const int64_t N = p->N, K = p->K, r = p->rank;
+  h->r_pad = rank_pad(r);
+  const HostPack& hp = h->host;
+  h->six_sgX = 6.0f * hp.s_gX;
+  h->inv_alpha = 1.0f / hp.alpha;
+
+  // ---- device layouts on the host
+  const int64_t KG = scale_groups(K);
+  const int64_t Npad = round_up(N, 256);
+  std::vector<uint8_t> sc_tiled(size_t(Npad / 128) * KG * 512, 0);
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t j = 0; j < K / 16; ++j)
+      sc_tiled[((n / 128) * KG + j / 4) * 512 + (n % 32) * 16 + ((n % 128) / 32) * 4 + (j % 4)] =
+          hp.R_scales[n * (K / 16) + j];
+  std::vector<uint16_t> l2t(size_t(N) * std::max<int64_t>(h->r_pad, 1), 0);
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t j = 0; j < r; ++j) l2t[n * h->r_pad + j] = hp.L2[j * N + n];
+  // L1' = diag(1/lambda) L1 in bf16, in the fragment order kernel 1 loads
+  const int64_t NT = r / 8;
+  std::vector<uint16_t> lperm(size_t(std::max<int64_t>(K * r, 1)), 0);
+  for (int64_t c = 0; c < K / 64; ++c)
+    for (int64_t nt = 0; nt < NT; ++nt)
+      for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane >> 2, t = lane & 3;
+        for (int i = 0; i < 16; ++i) {
+          const int64_t k = 64 * c + 16 * t + i, j = 8 * nt + g;
+          const double v = double(hp.inv_lambda[k]) * double(bf16_to_f32(hp.L1[k * r + j]));
+          lperm[(((c * NT + nt) * 32 + lane) * 16) + i] = f64_to_bf16(v);
+        }
+      }
+
+  // ---- upload
+  auto up = [&](void** dst, const void* src, size_t bytes) -> cudaError_t {
+    cudaError_t ee;
+    *dst = dalloc(bytes, &ee);
+    if (ee != cudaSuccess) return ee;
+    if (bytes) ee = cudaMemcpyAsync(*dst, src, bytes, cudaMemcpyHostToDevice, stream);
+    return ee;
+  };
+  e = up(reinterpret_cast<void**>(&h->d_R_codes), hp.R_codes.data(), hp.R_codes.size());
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_R_scales), sc_tiled.data(), sc_tiled.size());
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_L2t), l2t.data(), l2t.size() * 2);
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_Lperm), lperm.data(), lperm.size() * 2);
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_inv_lambda), hp.inv_lambda.data(), K * 4);
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_bias), hp.bias.data(), N * 2);
+  if (e == cudaSuccess) {
+    h->d_err = static_cast<int*>(dalloc(sizeof(int), &e));
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->d_err, 0, sizeof(int), stream);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    free_layer(h);
+    delete h;
+    return e == cudaErrorMemoryAllocation ? fail(SVDQ_ERR_OOM, "device allocation failed")
+                                          : cuda_fail(e, "uploading the packed layer");
+  }
+  if (!encode_map_2d(h->maps.B, 1, h->d_R_codes, K / 2, N, K / 2, 128, 256, 1, &err) ||
+      (r > 0 && !encode_map_2d(h->maps.L2, 2, h->d_L2t, h->r_pad, N, h->r_pad * 2, 64, 256, 1, &err))) {
+    free_layer(h);
+    delete h;
+    return fail(SVDQ_ERR_CUDA, err);
+  }
+  if (p->M_max > 0) {
+    s = svdq_reserve(h, p->M_max, 0);
+    if (s != SVDQ_OK) {
+      free_layer(h);
+      delete h;
+      return s;
+    }
+  }
+  *out = h;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_destroy(svdq_handle_t h) {
+  if (!h) return SVDQ_OK;
+  DeviceGuard guard(h->device);
+  cudaDeviceSynchronize();
+  free_layer(h);
+  delete h;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_get_info(svdq_handle_t h, svdq_info_t* info) {
+  if (!h || !info) return fail(SVDQ_ERR_INVALID_ARG, "null argument");
+  info->N = h->host.N;
+  info->K = h->host.K;
+  info->rank = h->host.rank;
+  info->r_pad = h->r_pad;
+  info->M_max = h->ws_M;
+  info->s_gW = h->host.s_gW;
+  info->s_gX = h->host.s_gX;
+  info->alpha = h->host.alpha;
+  info->device = h->device;
+  info->sm_count = h->sm_count;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_export(svdq_handle_t h, svdq_packed_host_t* out) {
+  if (!h || !out) return fail(SVDQ_ERR_INVALID_ARG, "null argument");
+  const HostPack& hp = h->host;
+  const int64_t N = hp.N, K = hp.K, r = hp.rank;
+  if (out->lambda) std::memcpy(out->lambda, hp.lambda.data(), sizeof(float) * K);
+  if (out->inv_lambda) std::memcpy(out->inv_lambda, hp.inv_lambda.data(), sizeof(float) * K);
+  if (out->L1_bf16 && r) std::memcpy(out->L1_bf16, hp.L1.data(), sizeof(uint16_t) * K * r);
+  if (out->L2_bf16 && r) std::memcpy(out->L2_bf16, hp.L2.data(), sizeof(uint16_t) * r * N);
+  if (out->R_codes) std::memcpy(out->R_codes, hp.R_codes.data(), hp.R_codes.size());
+  if (out->R_scales) std::memcpy(out->R_scales, hp.R_scales.data(), hp.R_scales.size());
+  if (out->bias_bf16) std::memcpy(out->bias_bf16, hp.bias.data(), sizeof(uint16_t) * N);
+  out->s_gW = hp.s_gW;
+  out->s_gX = hp.s_gX;
+  out->alpha = hp.alpha;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_workspace_size(svdq_handle_t h, int64_t M, int32_t host_staging, size_t* bytes) {
+  if (!h || !bytes || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null argument or negative M");
+  *bytes = ws_layout(h, M, host_staging != 0).total;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_reserve(svdq_handle_t h, int64_t M_max, int32_t host_staging) {
+  if (!h || M_max < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M_max");
+  DeviceGuard guard(h->device);
+  const size_t bytes = ws_layout(h, M_max, host_staging != 0).total;
+  cudaError_t e;
+  void* p = dalloc(bytes, &e);
+  if (e != cudaSuccess) return fail(SVDQ_ERR_OOM, "workspace allocation failed");
+  return attach_workspace(h, p, bytes, M_max, host_staging != 0, true, nullptr);
+}
+
+svdq_status_t svdq_set_workspace(svdq_handle_t h, void* dev_ptr, size_t bytes, int64_t M_max, int32_t host_staging) {
+  if (!h || M_max < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M_max");
+  DeviceGuard guard(h->device);
+  if (dev_ptr == nullptr) return attach_workspace(h, nullptr, 0, 0, false, false, nullptr);
+  if (reinterpret_cast<uintptr_t>(dev_ptr) & 255u) return fail(SVDQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (bytes < ws_layout(h, M_max, host_staging != 0).total)
+    return fail(SVDQ_ERR_WORKSPACE, "workspace smaller than svdq_workspace_size");
+  return attach_workspace(h, dev_ptr, bytes, M_max, host_staging != 0, false, nullptr);
+}
+
+svdq_status_t svdq_quantize_act(svdq_handle_t h, const void* X, int64_t M, void* x_codes, void* x_scales, void* T,
+                                void* stream) {
+  if (!h || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M");
+  if (M == 0) return SVDQ_OK;
+  if (!X || !x_codes || !x_scales || (h->host.rank > 0 && !T)) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!aligned16(X) || !aligned16(x_codes) || !aligned16(x_scales) || (T && !aligned16(T)))
+    return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (!h->ws || h->ws_M < M) return fail(SVDQ_ERR_WORKSPACE, "no workspace for this M (svdq_reserve)");
+  DeviceGuard guard(h->device);
+  return launch_k1(h, X, M, x_codes, x_scales, T, static_cast<cudaStream_t>(stream));
+}
+
+svdq_status_t svdq_gemm_quantized(svdq_handle_t h, const void* x_codes, const void* x_scales, const void* T, void* Y,
+                                  int64_t M, void* stream) {
+  if (!h || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M");
+  if (M == 0) return SVDQ_OK;
+  if (!x_codes || !x_scales || !Y || (h->host.rank > 0 && !T)) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!aligned16(x_codes) || !aligned16(x_scales) || !aligned16(Y) || (T && !aligned16(T)))
+    return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  DeviceGuard guard(h->device);
+  return launch_k2(h, x_codes, x_scales, T, Y, M, static_cast<cudaStream_t>(stream));
+}
+
+svdq_status_t svdq_linear_forward(svdq_handle_t h, const void* X, void* Y, int64_t M, void* stream) {
+  if (!h || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M");
+  if (M == 0) return SVDQ_OK;
+  if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (X == Y) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not alias");
+  if (!h->ws || h->ws_M < M) return fail(SVDQ_ERR_WORKSPACE, "no workspace for this M (svdq_reserve)");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
+  void* codes = h->ws + w.codes;
+  void* scales = h->ws + w.scales;
+  void* T = h->host.rank ? h->ws + w.T : nullptr;
+  svdq_status_t st = launch_k1(h, X, M, codes, scales, T, s);
+  if (st != SVDQ_OK) return st;
+  return launch_k2(h, codes, scales, T, Y, M, s);
+}
+
+svdq_status_t svdq_linear_forward_host(svdq_handle_t h, const uint16_t* X_host, uint16_t* Y_host, int64_t M,
+                                       void* stream) {
+  if (!h || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M");
+  if (M == 0) return SVDQ_OK;
+  if (!X_host || !Y_host) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!h->ws || !h->ws_staging || h->ws_M < M)
+    return fail(SVDQ_ERR_WORKSPACE, "needs a workspace reserved with host staging for this M");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout w = ws_layout(h, h->ws_M, true);
+  void* Xd = h->ws + w.Xs;
+  void* Yd = h->ws + w.Ys;
+  cudaError_t e = cudaMemcpyAsync(Xd, X_host, size_t(M) * h->host.K * 2, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "copying X to the device");
+  svdq_status_t st = svdq_linear_forward(h, Xd, Yd, M, stream);
+  if (st != SVDQ_OK) return st;
+  e = cudaMemcpyAsync(Y_host, Yd, size_t(M) * h->host.N * 2, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "copying Y to the host");
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_check_error(svdq_handle_t h) {
+  if (!h) return fail(SVDQ_ERR_INVALID_ARG, "null handle");
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronisation");
+  int v = 0;
+  e = cudaMemcpy(&v, h->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (v) return fail(SVDQ_ERR_TIMEOUT, "a kernel gave up a bounded wait (error word " + std::to_string(v) + ")");
+  return SVDQ_OK;
+}
+
+}  // extern "C"

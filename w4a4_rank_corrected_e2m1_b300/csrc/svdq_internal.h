@@ -1,0 +1,94 @@
+// Internal declarations shared by the host pack, the C-ABI layer and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/svdq.h"
+
+#ifdef __CUDACC__
+#define SVDQ_HD __host__ __device__
+#else
+#define SVDQ_HD
+#endif
+
+namespace svdq {
+
+// ------------------------------------------------------------------ host pack (pack_host.cpp)
+struct HostPack {
+  int64_t N = 0, K = 0, rank = 0;
+  std::vector<float> lambda, inv_lambda;   // K
+  std::vector<uint16_t> L1;                // K x rank (bf16 bits)
+  std::vector<uint16_t> L2;                // rank x N (bf16 bits)
+  std::vector<uint8_t> R_codes;            // N x K/2
+  std::vector<uint8_t> R_scales;           // N x K/16 (row-major, not tiled)
+  std::vector<uint16_t> bias;              // N
+  float s_gW = 1.f, s_gX = 1.f, alpha = 1.f;
+};
+
+// Validates p and runs smoothing, SVD, residual and NVFP4 quantisation on the CPU.
+svdq_status_t pack_on_host(const svdq_pack_params_t* p, HostPack* out, std::string* err);
+
+// Format helpers (host side).
+float bf16_to_f32(uint16_t b);
+uint16_t f64_to_bf16(double a);
+uint8_t e4m3_encode_nonneg(float s);
+float e4m3_decode(uint8_t b);
+uint8_t e2m1_encode(float v);
+
+// ------------------------------------------------------------------ device layouts
+SVDQ_HD inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+SVDQ_HD inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+// 64-column groups per 128-row block of a tiled scale buffer (padded to whole 256-column stages).
+SVDQ_HD inline int64_t scale_groups(int64_t K) { return 4 * ceil_div(K, 256); }
+SVDQ_HD inline int64_t rank_pad(int64_t r) { return r == 0 ? 0 : round_up(r, 64); }
+
+// ------------------------------------------------------------------ kernel 1 (k1_actquant.cu)
+struct K1Args {
+  const uint16_t* X;          // M x K bf16
+  const float* inv_lambda;    // K
+  const uint16_t* Lperm;      // folded + permuted L1 (see k1_actquant.cu), may be null if rank == 0
+  uint8_t* x_codes;           // M x K/2
+  uint8_t* x_scales;          // tiled
+  uint16_t* T;                // M x r_pad bf16 (null if rank == 0)
+  float* partial;             // split-K partial sums [nsplit][M_pad128][rank] fp32
+  unsigned int* counters;     // one per 128-row tile, zero between calls
+  int64_t M, K;
+  int rank, r_pad;
+  float s_gX, six_sgX, inv_alpha;
+};
+struct K1Plan {
+  int row_tiles = 0, nsplit = 1, chunks_per_split = 1;
+};
+K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count);
+size_t k1_partial_bytes(int64_t M, int64_t K, int rank, int sm_count);
+int k1_launch(const K1Args& a, const K1Plan& plan, void* stream);  // returns cudaError_t
+
+// ------------------------------------------------------------------ kernel 2 (k2_fp4gemm.cu)
+struct K2Maps {
+  alignas(64) unsigned char A[128];    // CUtensorMap: x codes      (u8, K/2 x M, box 128 x 128)
+  alignas(64) unsigned char B[128];    // CUtensorMap: R codes      (u8, K/2 x N, box 128 x 256)
+  alignas(64) unsigned char T[128];    // CUtensorMap: T            (bf16, r_pad x M, box 64 x 128)
+  alignas(64) unsigned char L2[128];   // CUtensorMap: L2^T         (bf16, r_pad x N, box 64 x 256)
+  alignas(64) unsigned char Y[128];    // CUtensorMap: Y            (bf16, N x M, box 64 x 32)
+};
+struct K2Args {
+  const uint8_t* sfa;         // tiled x scales
+  const uint8_t* sfb;         // tiled R scales (rows padded to 256)
+  const uint16_t* bias;       // N bf16
+  int* err;                   // device error word
+  int64_t M, N, K;
+  int rank;
+  float alpha;
+};
+int k2_launch(const K2Maps& maps, const K2Args& a, int sm_count, void* stream);
+size_t k2_smem_bytes();
+
+// Tensor-map encoding through the driver entry point (api.cu).
+bool encode_map_2d(void* map, int dtype_bytes, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle128,
+                   std::string* err);
+
+}  // namespace svdq
