@@ -60,24 +60,27 @@ def workload_flops(w, rows=None):
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def oracle_sample(w, d, budget_s=12.0, max_rows=None):
-    """Time the oracle forward on a bounded sample of rows; returns (TFLOP/s, rows, seconds, threads)."""
-    from threadpoolctl import threadpool_info
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except ImportError:
+        return len(os.sched_getaffinity(0))
+
+
+def oracle_sample(w, d, p, budget_s=10.0):
+    """Time the oracle forward on a bounded sample of rows of the workload, given a packed
+    layer p; returns (TFLOP/s, rows, seconds)."""
     from oracle import svdquant as sq
-    p = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"][: min(w.M, 1024)])
     rows = 16
-    best = None
     while True:
         t0 = time.perf_counter()
         sq.forward(d["X"][:rows], p)
         dt = time.perf_counter() - t0
-        best = (rows, dt)
-        if dt > budget_s / 4 or rows >= w.M or (max_rows and rows >= max_rows):
+        if dt > budget_s / 3 or rows >= w.M:
             break
         rows = min(w.M, rows * 4)
-    rows, dt = best
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-    return workload_flops(w, rows) / dt / 1e12, rows, dt, threads
+    return workload_flops(w, rows) / dt / 1e12, rows, dt
 
 
 def run_reference(args, w):
@@ -85,9 +88,8 @@ def run_reference(args, w):
     if rank != 0:
         return
     d = synthetic.make(w)
-    from threadpoolctl import threadpool_info
     from oracle import svdquant as sq
-    p = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"][: min(w.M, 1024)])
+    p = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"])
     rows = min(w.M, 128)
     for _ in range(args.warmup):
         sq.forward(d["X"][:rows], p)
@@ -98,7 +100,7 @@ def run_reference(args, w):
         times.append(time.perf_counter() - t0)
     tot = sum(times)
     val = workload_flops(w, rows) * args.steps / tot / 1e12
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    threads = blas_threads()
     sample = f"{rows} of {w.M} token rows per step (oracle forward, weights pre-packed)"
     out = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
@@ -287,10 +289,14 @@ def run_ours(args, w):
             "pack_s": t_pack,
         }
         if not args.no_cpu_baseline:
-            v, rows, dt, threads = oracle_sample(w, d)
+            exp = layer.export()
+            rc = exp["R_codes"]
+            exp["R_codes"] = np.stack([rc & 0xF, rc >> 4], axis=-1).reshape(rc.shape[0], -1)
+            v, rows, dt = oracle_sample(w, d, exp)
+            threads = blas_threads()
             out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
                                    "threads": threads, "kind": "oracle",
-                                   "sample": f"oracle forward on {rows} of {M} token rows, {dt:.2f} s"}
+                                   "sample": f"oracle forward on {rows} of {M} token rows ({dt:.2f} s) with the layer's packed operands"}
         print(json.dumps(out), flush=True)
     layer.close()
     layer0.close()

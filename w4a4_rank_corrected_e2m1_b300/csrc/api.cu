@@ -217,13 +217,12 @@ svdq_status_t launch_k2(svdq_layer* h, const void* codes, const void* scales, co
   K2Maps maps = h->maps;
   std::string err;
   if (!encode_map_2d(maps.A, 1, codes, K / 2, M, K / 2, 128, 128, 1, &err) ||
+      !encode_map_2d(maps.SFA, 1, scales, 256, svdq_scales_bytes(M, K) / 256, 256, 256, 8, 0, &err) ||
       !encode_map_2d(maps.Y, 2, Y, N, M, N * 2, 64, 32, 1, &err))
     return fail(SVDQ_ERR_CUDA, err);
   if (h->host.rank > 0 && !encode_map_2d(maps.T, 2, T, h->r_pad, M, h->r_pad * 2, 64, 128, 1, &err))
     return fail(SVDQ_ERR_CUDA, err);
   K2Args a{};
-  a.sfa = static_cast<const uint8_t*>(scales);
-  a.sfb = h->d_R_scales;
   a.bias = h->d_bias;
   a.err = h->d_err;
   a.M = M;
@@ -364,8 +363,9 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
     return e == cudaErrorMemoryAllocation ? fail(SVDQ_ERR_OOM, "device allocation failed")
                                           : cuda_fail(e, "uploading the packed layer");
   }
-  if (!encode_map_2d(h->maps.B, 1, h->d_R_codes, K / 2, N, K / 2, 128, 256, 1, &err) ||
-      (r > 0 && !encode_map_2d(h->maps.L2, 2, h->d_L2t, h->r_pad, N, h->r_pad * 2, 64, 256, 1, &err))) {
+  if (!encode_map_2d(h->maps.B, 1, h->d_R_codes, K / 2, N, K / 2, 128, 128, 1, &err) ||
+      !encode_map_2d(h->maps.SFB, 1, h->d_R_scales, 256, int64_t(sc_tiled.size()) / 256, 256, 256, 8, 0, &err) ||
+      (r > 0 && !encode_map_2d(h->maps.L2, 2, h->d_L2t, h->r_pad, N, h->r_pad * 2, 64, 128, 1, &err))) {
     free_layer(h);
     delete h;
     return fail(SVDQ_ERR_CUDA, err);

@@ -10,7 +10,9 @@
 // 16*MT rows.  Thread (g = lane/4, t = lane%4) loads, for each of its rows, the 16
 // consecutive bf16 at columns 16t..16t+15 of the chunk (two 16-byte loads): exactly one
 // NVFP4 block, so the block maximum needs no shuffles, and a quad writes 32 contiguous
-// bytes of codes per row.
+// bytes of codes per row.  The E2M1 conversion (cvt.rn.satfinite.e2m1x2) rounds to nearest
+// even and keeps the sign of a negative value that rounds to zero, which is the format rule
+// the codes follow.
 //
 // Down-projection on the warp MMA (m16n8k16, bf16 in, f32 accumulate).  The registers a
 // thread already holds are used directly as A fragments: the k order inside each 16-wide
@@ -33,15 +35,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-
-// Nibble sign mask of 8 consecutive bf16 held as 4 words (element 2i low half of word i):
-// bit 4e+3 set where element e has its sign bit set.
-__device__ __forceinline__ uint32_t sign_nibbles(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
-  // top bytes: even elements live in byte 1 of each word, odd elements in byte 3
-  const uint32_t ev = __byte_perm(__byte_perm(w0, w1, 0x0051), __byte_perm(w2, w3, 0x0051), 0x5410);
-  const uint32_t od = __byte_perm(__byte_perm(w0, w1, 0x0073), __byte_perm(w2, w3, 0x0073), 0x5410);
-  return ((ev >> 4) & 0x08080808u) | (od & 0x80808080u);
-}
 
 template <int NT, int MT>
 __global__ void __launch_bounds__(kWarps * 32) k1_kernel(K1Args a, int chunks_per_split, int nsplit) {
@@ -124,11 +117,9 @@ __global__ void __launch_bounds__(kWarps * 32) k1_kernel(K1Args a, int chunks_pe
           const float rcp = __frcp_rn(d);
           float q[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) q[i] = fabsf(__fmul_rn(xh[h][i], rcp));
+          for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(xh[h][i], rcp);
           code0 = ptx::cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
           code1 = ptx::cvt_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
-          code0 |= sign_nibbles(w[r][0], w[r][1], w[r][2], w[r][3]);
-          code1 |= sign_nibbles(w[r][4], w[r][5], w[r][6], w[r][7]);
         }
         if (row < M) {
           uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + col / 2);
