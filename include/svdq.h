@@ -198,6 +198,26 @@ svdq_status_t svdq_linear_forward_host(svdq_handle_t h, const uint16_t* X_host, 
                                        int64_t M, void* stream);
 
 /*
+ * svdq_linear_forward_noalloc -- the same layer as svdq_linear_forward for callers that must
+ * not allocate device memory when they run it: code inside a framework's memory pool or budget,
+ * code recorded into a CUDA graph, latency-critical loops that cannot take cudaMalloc's implicit
+ * synchronisation.  Instead of the handle's workspace it uses a statically sized scratch array
+ * that the library holds on every device it is loaded on (32 MiB per device, kept until the
+ * process exits), so the call makes no allocation of any kind.  It is not described by the
+ * SVDQuant/Nunchaku pages; it is an interface convenience of this library.
+ *   X: device M x K bf16, Y: device M x N bf16 (as svdq_linear_forward).
+ *   The first call on a device looks up the scratch array's device address (once per device,
+ *   with that device current); make that first call before any stream capture.
+ *   Every call shares the one scratch array: calls that overlap on the GPU (different streams,
+ *   or different handles on the same device without ordering) race on it.  Order them on one
+ *   stream.
+ *   Errors: SVDQ_ERR_WORKSPACE when M needs more scratch than 32 MiB (svdq_workspace_size with
+ *   host_staging = 0 gives the requirement), plus the errors of svdq_linear_forward.
+ */
+svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void* X_bf16, void* Y_bf16, int64_t M,
+                                          void* stream);
+
+/*
  * svdq_check_error -- synchronises the handle's device, reads and clears the
  * device error word that the kernels set when a bounded wait gives up.
  * Returns SVDQ_OK or SVDQ_ERR_TIMEOUT (or SVDQ_ERR_CUDA for a sticky CUDA error).

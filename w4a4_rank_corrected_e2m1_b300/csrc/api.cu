@@ -526,3 +526,76 @@ svdq_status_t svdq_check_error(svdq_handle_t h) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ forward without allocation
+// Some callers cannot allocate device memory at the point where they run a layer: code running
+// under a framework's memory pool or budget (where a library-owned cudaMalloc would bypass the
+// pool and may not fit), code recorded into a CUDA graph (where cudaMalloc is not a capturable
+// operation), or latency-critical loops where cudaMalloc's implicit device synchronisation is not
+// acceptable.  svdq_linear_forward_noalloc serves them: its scratch (quantised activations, T,
+// the split-K partial sums and their counters) lives in one statically sized device array that
+// the library holds on every device it is loaded on, so the call itself allocates nothing.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB per device
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {nullptr};
+
+// Device address of g_static_scratch on the current device (looked up once per device).
+svdq_status_t static_scratch(int device, unsigned char** out) {
+  if (device < 0 || device >= 64) return fail(SVDQ_ERR_INVALID_ARG, "device ordinal out of range");
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
+    g_static_ptr[device] = p;
+  }
+  *out = static_cast<unsigned char*>(g_static_ptr[device]);
+  return SVDQ_OK;
+}
+
+}  // namespace
+
+extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void* X, void* Y, int64_t M,
+                                                     void* stream) {
+  if (!h || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M");
+  if (M == 0) return SVDQ_OK;
+  if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (X == Y) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not alias");
+  const WsLayout w = ws_layout(h, M, false);
+  if (w.total > kStaticScratchBytes)
+    return fail(SVDQ_ERR_WORKSPACE, "M = " + std::to_string(M) + " needs " + std::to_string(w.total) +
+                                        " bytes of scratch; the static scratch holds " +
+                                        std::to_string(kStaticScratchBytes) + " bytes");
+  DeviceGuard guard(h->device);
+  unsigned char* ws = nullptr;
+  svdq_status_t st = static_scratch(h->device, &ws);
+  if (st != SVDQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the split-K counters must start at zero; the previous call's contents are still there
+  cudaError_t e = cudaMemsetAsync(ws + w.counters, 0, w.Xs - w.counters, s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch counters");
+  K1Args a{};
+  a.X = static_cast<const uint16_t*>(X);
+  a.inv_lambda = h->d_inv_lambda;
+  a.Lperm = h->d_Lperm;
+  a.x_codes = ws + w.codes;
+  a.x_scales = ws + w.scales;
+  a.T = h->host.rank ? reinterpret_cast<uint16_t*>(ws + w.T) : nullptr;
+  a.partial = reinterpret_cast<float*>(ws + w.partial);
+  a.counters = reinterpret_cast<unsigned int*>(ws + w.counters);
+  a.M = M;
+  a.K = h->host.K;
+  a.rank = int(h->host.rank);
+  a.r_pad = int(h->r_pad);
+  a.s_gX = h->host.s_gX;
+  a.six_sgX = h->six_sgX;
+  a.inv_alpha = h->inv_alpha;
+  const int e1 = k1_launch(a, k1_plan(M, a.K, a.rank, h->sm_count), s);
+  if (e1 != 0) return cuda_fail(cudaError_t(e1), "kernel 1 launch");
+  return launch_k2(h, a.x_codes, a.x_scales, a.T, Y, M, s);
+}
