@@ -11,8 +11,9 @@ article):
          W^T ~= L1 L2  (L1: K x r, L2: r x N, both bfloat16)
   3. residual: R = W^ - (L1 L2)^T, quantised to 4 bit (NVFP4); activations
      X^ are quantised to 4 bit at run time
-  4. two-branch forward ("a compact high precision low rank path" plus "a
-     dominant 4 bit path"):
+  4. two-branch forward: a small 16-bit low-rank branch that absorbs the
+     hardest part of the weight distribution, summed with a 4-bit branch that
+     does most of the arithmetic:
          Y = Q4(X^) Q4(R)^T + (X^ L1) L2 + b
 
 Readings where the pages are silent (each also listed in the design notes):
