@@ -38,7 +38,7 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="flux_mlp_up", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -116,42 +116,107 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ clocks
+class _Nvml:
+    """The few NVML calls the sampler needs, through ctypes on the driver's libnvidia-ml."""
+
+    CLOCK_SM = 1
+
+    def __init__(self, cuda_index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        n = ctypes.c_uint()
+        self.lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+        idx = cuda_index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        if n.value == 1:
+            idx = 0
+        elif vis and all(v.strip().isdigit() for v in vis.split(",")):
+            idx = int(vis.split(",")[cuda_index])
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def max_sm(self):
+        v = self.ct.c_uint()
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.ct.byref(v)) == 0 else None
+
+    def sample(self):
+        sm, rs = self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, self.ct.byref(sm)) != 0:
+            return None
+        if self.reasons_fn(self.h, self.ct.byref(rs)) != 0:
+            return None
+        return sm.value, rs.value
+
+
 class Clocks:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """SM clock and throttle reasons sampled during the timed region.
+
+    NVML (the library nvidia-smi reads, through ctypes) polled about every half millisecond
+    from a thread, so that short timed regions still get samples; falls back to
+    `nvidia-smi --query-gpu ... -lms 100`."""
+
+    REASONS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
 
     def __init__(self, device_index):
-        self.dev = device_index
-        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        import threading
+        self.samples = []
+        self.stop_ev = threading.Event()
+        self.proc = None
         try:
-            self.p = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
-                                      stdout=self.f, stderr=subprocess.DEVNULL)
+            nv = _Nvml(device_index)
+            self.max_mhz = nv.max_sm()
+
+            def run():
+                while not self.stop_ev.is_set():
+                    x = nv.sample()
+                    if x is not None:
+                        self.samples.append(x)
+                    time.sleep(0.0005)
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
         except Exception:
-            self.p = None
+            self.thread = None
+            self.max_mhz = None
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(device_index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=self.f, stderr=subprocess.DEVNULL)
+            except Exception:
+                self.proc = None
 
     def stop(self):
-        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
-        if self.p is None:
+        out = {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        if self.thread is not None:
+            self.stop_ev.set()
+            self.thread.join()
+            out["source"] = "nvml"
+            if self.samples:
+                sm = [x[0] for x in self.samples]
+                mask = 0
+                for x in self.samples:
+                    mask |= x[1]
+                out.update(sm_mhz=statistics.median(sm), samples=len(sm),
+                           reasons=sorted(n for n, b in self.REASONS.items() if mask & b))
             return out
-        self.p.terminate()
-        self.p.wait()
-        self.f.flush()
-        rows = []
-        for line in open(self.f.name):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
-        os.unlink(self.f.name)
-        if not rows:
-            return out
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
-        out.update(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
-                   reasons=reasons, samples=len(rows))
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.flush()
+            rows = [[x.strip() for x in line.split(",")] for line in open(self.f.name)]
+            os.unlink(self.f.name)
+            sm = [float(r[0]) for r in rows if r and r[0].replace(".", "").isdigit()]
+            mx = [float(r[1]) for r in rows if len(r) > 1 and r[1].replace(".", "").isdigit()]
+            out.update(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                       samples=len(sm), source="nvidia-smi")
         return out
 
 

@@ -146,7 +146,8 @@ int64_t svdq_scales_bytes(int64_t M, int64_t K);
 
 /*
  * Workspace: the forward keeps the quantised activations, T and the split-K
- * partial sums of the down-projection in a device workspace.
+ * partial sums of the down-projection in a device workspace (no part of it
+ * needs clearing by the caller).
  * svdq_workspace_size gives the bytes needed for M rows; svdq_reserve makes the
  * handle allocate (cudaMalloc) and own one for M <= M_max; svdq_set_workspace
  * lends caller memory instead (256-byte aligned, NULL to drop it).  With
@@ -165,7 +166,8 @@ svdq_status_t svdq_set_workspace(svdq_handle_t h, void* dev_ptr, size_t bytes, i
  * format rules above) and T = X^ L1 / alpha (low-rank down-projection of stage
  * two, float32 accumulation, bfloat16 out).  X: device M x K bf16.  x_codes,
  * x_scales, T: device buffers in the layouts above (T may be NULL when
- * rank == 0).  Uses the handle's workspace for split-K partials.
+ * rank == 0).  Uses the handle's workspace for the split-K partial sums.
+ * Scale bytes of the groups past K (K not a multiple of 256) are written as zero.
  */
 svdq_status_t svdq_quantize_act(svdq_handle_t h, const void* X_bf16, int64_t M, void* x_codes,
                                 void* x_scales, void* T_bf16, void* stream);
@@ -173,8 +175,8 @@ svdq_status_t svdq_quantize_act(svdq_handle_t h, const void* X_bf16, int64_t M, 
 /*
  * svdq_gemm_quantized -- kernel 2 alone on already-quantised activations:
  * Y = alpha * (acc_fp4 + T L2) + b with the block-scaled FP4 tensor-core GEMM
- * (the "dominant 4 bit path") and the low-rank up-projection added into the
- * same accumulator.  Inputs in the layouts above; Y: device M x N bf16, fully
+ * (the 4-bit branch) and the low-rank up-projection added into the same
+ * accumulator.  Inputs in the layouts above; Y: device M x N bf16, fully
  * overwritten, written once.
  */
 svdq_status_t svdq_gemm_quantized(svdq_handle_t h, const void* x_codes, const void* x_scales,

@@ -38,7 +38,8 @@ def case(w: synthetic.Workload, **pack_kw):
 def run_k1(layer, X, M):
     K = layer.K
     codes = torch.empty((max(M, 1), K // 2), dtype=torch.uint8, device="cuda")
-    scales = torch.zeros(max(svdq.scales_bytes(M, K), 16), dtype=torch.uint8, device="cuda")
+    # 0xFF is an E4M3 NaN: any byte kernel 1 leaves unwritten shows up in the comparisons
+    scales = torch.full((max(svdq.scales_bytes(M, K), 16),), 0xFF, dtype=torch.uint8, device="cuda")
     r_pad = layer.info.r_pad
     T = torch.empty((max(M, 1), max(r_pad, 8)), dtype=torch.int16, device="cuda") if layer.rank else None
     Xd = gh.dev_u16(X)
@@ -105,6 +106,37 @@ def test_k1_rounding_edges():
     bad = np.argwhere(c != rc)
     assert bad.size == 0, [(int(i), int(j), float(sq.bf16_to_f64(X[i, j])), int(c[i, j]), int(rc[i, j])) for i, j in bad[:8]]
     assert np.all(rc[0, :16] == nvfp4.e2m1_encode(np.float32(ties)))
+
+
+def test_k1_scale_code_boundaries():
+    """Block maxima exactly at every E4M3 rounding midpoint (times 6, so that with s_gX = 1 the
+    raw scale amax / 6 is the midpoint itself) and one bf16 step to either side."""
+    from oracle import nvfp4 as nv
+    vals = nv.e4m3_decode(np.arange(0, 127, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2
+    amax = np.concatenate([6 * mids, 6 * vals[1:]])
+    bits = synthetic.f64_to_bf16_bits(amax)
+    cand = np.concatenate([bits, bits + np.uint16(1), bits - np.uint16(1)])
+    amaxv = sq.bf16_to_f64(cand)
+    amaxv = amaxv[(amaxv > 0) & (amaxv < 6 * 448)]
+    rng = np.random.default_rng(9)
+    K = 256
+    nblk = len(amaxv)
+    rows = int(np.ceil(nblk / (K // 16)))
+    X = np.zeros((rows, K))
+    for b, am in enumerate(amaxv):
+        r, j = divmod(b, K // 16)
+        blk = rng.uniform(-1, 1, 16) * am * 0.9
+        blk[rng.integers(16)] = am if rng.random() < 0.5 else -am
+        X[r, 16 * j:16 * j + 16] = blk
+    Xb = synthetic.f64_to_bf16_bits(X)
+    W = synthetic.f64_to_bf16_bits(rng.standard_normal((64, K)) / 16)
+    layer = svdq.Layer(W, 0, smooth=False, s_gX=1.0, M_max=rows)
+    exp = layer.export()
+    c, s, _, _ = run_k1(layer, Xb, rows)
+    rc, rs, _ = sq.quantize_act(Xb, exp["inv_lambda"], exp["s_gX"])
+    assert np.array_equal(s, rs), f"scale mismatches {np.sum(s != rs)}"
+    assert np.array_equal(c, rc)
 
 
 @pytest.mark.parametrize("w", PARITY, ids=lambda w: w.name)
@@ -235,9 +267,13 @@ def test_ragged_n_and_k():
     """N not a multiple of the 256-wide tile and K not a multiple of the 256-wide stage."""
     w = synthetic.scaled(synthetic.QKV, name="ragged", M=200, K=320, N=272, rank=16, n_outlier=3)
     d, layer, exp = case(w)
-    c, s, _, _ = run_k1(layer, d["X"], w.M)
+    c, s, _, raw = run_k1(layer, d["X"], w.M)
     rc, rs, _ = sq.quantize_act(d["X"], exp["inv_lambda"], exp["s_gX"])
     assert np.array_equal(c, rc) and np.array_equal(s, rs)
+    # scale groups past K (K = 320: groups 5..7 of each 128-row tile) must be zero scales
+    KG = 4 * -(-w.K // 256)
+    tiles = raw[: -(-w.M // 128) * KG * 512].reshape(-1, KG, 512)
+    assert np.all(tiles[:, w.K // 64:, :] == 0)
     Y = run_forward(layer, d["X"], w.M)
     gh.assert_y_close(Y, sq.forward(d["X"], gh.oracle_packed(exp)), "ragged")
 

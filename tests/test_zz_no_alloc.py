@@ -56,7 +56,7 @@ def test_noalloc_rejects_sizes_beyond_the_static_scratch():
     layer = svdq.Layer(W, 32, s_gX=1.0)
     X = torch.zeros((8, K), dtype=torch.int16, device="cuda")
     Y = torch.zeros((8, N), dtype=torch.int16, device="cuda")
-    M_big = 16384                                   # needs well over 32 MiB of scratch
+    M_big = 32768                                   # needs well over 32 MiB of scratch
     assert layer.workspace_size(M_big) > (32 << 20)
     assert _forward_noalloc(layer, X, Y, M_big) == svdq.ERR_WORKSPACE
     assert b"static scratch" in svdq.LIB.svdq_last_error()

@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 #include <string>
@@ -103,8 +104,9 @@ struct svdq_layer {
   uint8_t* d_R_codes = nullptr;
   uint8_t* d_R_scales = nullptr;   // tiled, rows padded to 256
   uint16_t* d_L2t = nullptr;       // N x r_pad
-  uint16_t* d_Lperm = nullptr;     // folded + permuted L1
+  unsigned char* d_LI = nullptr;   // per chunk: folded + permuted L1 slice, then 1/lambda slice
   float* d_inv_lambda = nullptr;
+  float* d_qtab = nullptr;         // activation quantiser tables (thresholds, reciprocals)
   uint16_t* d_bias = nullptr;
   int* d_err = nullptr;
   K2Maps maps{};                   // B and L2 filled at pack
@@ -114,13 +116,13 @@ struct svdq_layer {
   bool ws_owned = false;
   int64_t ws_M = 0;
   bool ws_staging = false;
-  float six_sgX = 6.f, inv_alpha = 1.f;
+  float inv_six = 1.f / 6.f, inv_alpha = 1.f;
 };
 
 namespace {
 
 struct WsLayout {
-  size_t codes, scales, T, partial, counters, Xs, Ys, total;
+  size_t codes, scales, T, partial, arrivals, Xs, Ys, total;
 };
 
 WsLayout ws_layout(const svdq_layer* h, int64_t M, bool staging) {
@@ -130,11 +132,8 @@ WsLayout ws_layout(const svdq_layer* h, int64_t M, bool staging) {
   w.codes = off; off += align256(size_t(M) * K / 2);
   w.scales = off; off += align256(size_t(svdq_scales_bytes(M, K)));
   w.T = off; off += align256(size_t(M) * h->r_pad * 2);
-  // split-K partial sums: bounded over every M' <= M by (3 * SMs + row tiles) row tiles
-  const int64_t rows = r > 64 ? 64 : 128;
-  const int64_t tiles = ceil_div(M, rows);
-  w.partial = off; off += align256(r ? size_t(3 * h->sm_count + tiles) * rows * r * sizeof(float) : 0);
-  w.counters = off; off += align256(size_t(tiles + 1) * sizeof(unsigned int));
+  w.partial = off; off += align256(k1_partial_bytes(M, int(r)));
+  w.arrivals = off; off += align256(r ? k1_arrival_bytes(M) : 0);
   w.Xs = off; off += staging ? align256(size_t(M) * K * 2) : 0;
   w.Ys = off; off += staging ? align256(size_t(M) * N * 2) : 0;
   w.total = off;
@@ -162,8 +161,9 @@ void free_layer(svdq_layer* h) {
   cudaFree(h->d_R_codes);
   cudaFree(h->d_R_scales);
   cudaFree(h->d_L2t);
-  cudaFree(h->d_Lperm);
+  cudaFree(h->d_LI);
   cudaFree(h->d_inv_lambda);
+  cudaFree(h->d_qtab);
   cudaFree(h->d_bias);
   cudaFree(h->d_err);
   if (h->ws_owned) cudaFree(h->ws);
@@ -177,36 +177,41 @@ svdq_status_t attach_workspace(svdq_layer* h, void* ptr, size_t bytes, int64_t M
   h->ws_owned = owned;
   h->ws_M = ptr ? M_max : 0;
   h->ws_staging = ptr ? staging : false;
-  if (ptr) {
-    const WsLayout w = ws_layout(h, M_max, staging);
-    cudaError_t e = cudaMemsetAsync(h->ws + w.counters, 0, w.Xs - w.counters, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing workspace counters");
-  }
+  (void)stream;
   return SVDQ_OK;
+}
+
+// Kernel 1 launches draw a process-wide unique epoch for their split-K arrival words.
+std::atomic<unsigned long long> g_k1_epoch{1};
+
+void k1_scratch(K1Args* a, unsigned char* ws, const WsLayout& w) {
+  a->partial = reinterpret_cast<float*>(ws + w.partial);
+  a->arrivals = reinterpret_cast<unsigned long long*>(ws + w.arrivals);
+  a->epoch = g_k1_epoch.fetch_add(1) & ((1ull << 56) - 1);
 }
 
 svdq_status_t launch_k1(svdq_layer* h, const void* X, int64_t M, void* codes, void* scales, void* T,
                         cudaStream_t stream) {
-  const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
   K1Args a{};
+  k1_scratch(&a, h->ws, ws_layout(h, h->ws_M, h->ws_staging));
   a.X = static_cast<const uint16_t*>(X);
-  a.inv_lambda = h->d_inv_lambda;
-  a.Lperm = h->d_Lperm;
+  a.LI = h->d_LI;
   a.x_codes = static_cast<uint8_t*>(codes);
   a.x_scales = static_cast<uint8_t*>(scales);
   a.T = static_cast<uint16_t*>(T);
-  a.partial = reinterpret_cast<float*>(h->ws + w.partial);
-  a.counters = reinterpret_cast<unsigned int*>(h->ws + w.counters);
   a.M = M;
   a.K = h->host.K;
   a.rank = int(h->host.rank);
   a.r_pad = int(h->r_pad);
   a.s_gX = h->host.s_gX;
-  a.six_sgX = h->six_sgX;
+  a.inv_six = h->inv_six;
   a.inv_alpha = h->inv_alpha;
+  a.qtab = h->d_qtab;
+  a.err = h->d_err;
   const K1Plan plan = k1_plan(M, a.K, a.rank, h->sm_count);
-  const int e = k1_launch(a, plan, stream);
+  std::string err;
+  const int e = k1_launch(a, plan, stream, &err);
+  if (e == -1) return fail(SVDQ_ERR_CUDA, err);
   if (e != 0) return cuda_fail(cudaError_t(e), "kernel 1 launch");
   return SVDQ_OK;
 }
@@ -310,8 +315,10 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
   const int64_t N = p->N, K = p->K, r = p->rank;
   h->r_pad = rank_pad(r);
   const HostPack& hp = h->host;
-  h->six_sgX = 6.0f * hp.s_gX;
+  h->inv_six = 1.0f / (6.0f * hp.s_gX);
   h->inv_alpha = 1.0f / hp.alpha;
+  std::vector<float> qtab(256);
+  act_quant_tables(hp.s_gX, qtab.data(), qtab.data() + 128);
 
   // ---- device layouts on the host
   const int64_t KG = scale_groups(K);
@@ -324,19 +331,24 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
   std::vector<uint16_t> l2t(size_t(N) * std::max<int64_t>(h->r_pad, 1), 0);
   for (int64_t n = 0; n < N; ++n)
     for (int64_t j = 0; j < r; ++j) l2t[n * h->r_pad + j] = hp.L2[j * N + n];
-  // L1' = diag(1/lambda) L1 in bf16, in the fragment order kernel 1 loads
-  const int64_t NT = r / 8;
-  std::vector<uint16_t> lperm(size_t(std::max<int64_t>(K * r, 1)), 0);
-  for (int64_t c = 0; c < K / 64; ++c)
-    for (int64_t nt = 0; nt < NT; ++nt)
-      for (int lane = 0; lane < 32; ++lane) {
-        const int g = lane >> 2, t = lane & 3;
-        for (int i = 0; i < 16; ++i) {
-          const int64_t k = 64 * c + 16 * t + i, j = 8 * nt + g;
-          const double v = double(hp.inv_lambda[k]) * double(bf16_to_f32(hp.L1[k * r + j]));
-          lperm[(((c * NT + nt) * 32 + lane) * 16) + i] = f64_to_bf16(v);
-        }
+  // per 64-column chunk c: L1' = diag(1/lambda) L1 in bf16, transposed to rank rows of 64
+  // K-values (128 bytes, K-major) and laid out with the 128-byte swizzle the tensor cores read
+  // (16-byte unit u of row j stored at unit u ^ (j % 8)), followed by the chunk's 64 values of
+  // 1/lambda as float32
+  const int64_t l_bytes = r * 128;
+  const int64_t li_chunk = l_bytes + 256;
+  std::vector<unsigned char> li(size_t(K / 64) * li_chunk, 0);
+  for (int64_t c = 0; c < K / 64; ++c) {
+    unsigned char* base = li.data() + c * li_chunk;
+    for (int64_t j = 0; j < r; ++j)
+      for (int i = 0; i < 64; ++i) {
+        const int64_t k = 64 * c + i;
+        const double v = double(hp.inv_lambda[k]) * double(bf16_to_f32(hp.L1[k * r + j]));
+        const int unit = (i / 8) ^ int(j % 8);
+        reinterpret_cast<uint16_t*>(base + j * 128 + unit * 16)[i % 8] = f64_to_bf16(v);
       }
+    std::memcpy(base + l_bytes, hp.inv_lambda.data() + 64 * c, 256);
+  }
 
   // ---- upload
   auto up = [&](void** dst, const void* src, size_t bytes) -> cudaError_t {
@@ -349,8 +361,9 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
   e = up(reinterpret_cast<void**>(&h->d_R_codes), hp.R_codes.data(), hp.R_codes.size());
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_R_scales), sc_tiled.data(), sc_tiled.size());
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_L2t), l2t.data(), l2t.size() * 2);
-  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_Lperm), lperm.data(), lperm.size() * 2);
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_LI), li.data(), li.size());
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_inv_lambda), hp.inv_lambda.data(), K * 4);
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_qtab), qtab.data(), qtab.size() * 4);
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_bias), hp.bias.data(), N * 2);
   if (e == cudaSuccess) {
     h->d_err = static_cast<int*>(dalloc(sizeof(int), &e));
@@ -532,9 +545,12 @@ svdq_status_t svdq_check_error(svdq_handle_t h) {
 // under a framework's memory pool or budget (where a library-owned cudaMalloc would bypass the
 // pool and may not fit), code recorded into a CUDA graph (where cudaMalloc is not a capturable
 // operation), or latency-critical loops where cudaMalloc's implicit device synchronisation is not
-// acceptable.  svdq_linear_forward_noalloc serves them: its scratch (quantised activations, T,
-// the split-K partial sums and their counters) lives in one statically sized device array that
-// the library holds on every device it is loaded on, so the call itself allocates nothing.
+// acceptable.  svdq_linear_forward_noalloc serves them: its scratch (quantised activations, T and
+// kernel 1's split-K partial sums and arrival words) lives in one statically sized device array
+// that the library holds on every device it is loaded on, so the call itself allocates nothing.
+// Nothing in it needs clearing between calls: kernel 2 reads only bytes kernel 1 wrote earlier in
+// the same call, and the arrival words carry a per-launch epoch that makes stale contents
+// (another layer's, or an aborted call's) restart the count.
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB per device
@@ -576,26 +592,25 @@ extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void
   svdq_status_t st = static_scratch(h->device, &ws);
   if (st != SVDQ_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the split-K counters must start at zero; the previous call's contents are still there
-  cudaError_t e = cudaMemsetAsync(ws + w.counters, 0, w.Xs - w.counters, s);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch counters");
   K1Args a{};
+  k1_scratch(&a, ws, w);
   a.X = static_cast<const uint16_t*>(X);
-  a.inv_lambda = h->d_inv_lambda;
-  a.Lperm = h->d_Lperm;
+  a.LI = h->d_LI;
   a.x_codes = ws + w.codes;
   a.x_scales = ws + w.scales;
   a.T = h->host.rank ? reinterpret_cast<uint16_t*>(ws + w.T) : nullptr;
-  a.partial = reinterpret_cast<float*>(ws + w.partial);
-  a.counters = reinterpret_cast<unsigned int*>(ws + w.counters);
   a.M = M;
   a.K = h->host.K;
   a.rank = int(h->host.rank);
   a.r_pad = int(h->r_pad);
   a.s_gX = h->host.s_gX;
-  a.six_sgX = h->six_sgX;
+  a.inv_six = h->inv_six;
   a.inv_alpha = h->inv_alpha;
-  const int e1 = k1_launch(a, k1_plan(M, a.K, a.rank, h->sm_count), s);
+  a.qtab = h->d_qtab;
+  a.err = h->d_err;
+  std::string err;
+  const int e1 = k1_launch(a, k1_plan(M, a.K, a.rank, h->sm_count), s, &err);
+  if (e1 == -1) return fail(SVDQ_ERR_CUDA, err);
   if (e1 != 0) return cuda_fail(cudaError_t(e1), "kernel 1 launch");
   return launch_k2(h, a.x_codes, a.x_scales, a.T, Y, M, s);
 }

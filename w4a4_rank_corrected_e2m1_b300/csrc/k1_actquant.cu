@@ -2,28 +2,42 @@
 //   (a) smooths them, x^ = fl32(x * inv_lambda)            (stage one of SVDQuant),
 //   (b) quantises x^ to NVFP4: one E4M3 scale per 16 elements, E2M1 codes (stage three),
 //   (c) computes the low-rank down-projection T = X^ L1 of the 16-bit branch (stage two),
-// so X is read from HBM exactly once ("the low rank branch and the 4 bit branch ... share
-// inputs", Nunchaku section of the aiflownews article on Nunchaku in Diffusers).
+// so X is read from HBM exactly once: both branches of the layer consume the same smoothed
+// input, which the Nunchaku section of the aiflownews article on Nunchaku in Diffusers gives
+// as the reason to fuse them.
 //
-// Work decomposition: a CTA owns a tile of rows (128, or 64 for rank > 64) and a range of
-// 64-column chunks; splitting K across CTAs keeps all SMs busy at small M.  A warp owns
-// 16*MT rows.  Thread (g = lane/4, t = lane%4) loads, for each of its rows, the 16
-// consecutive bf16 at columns 16t..16t+15 of the chunk (two 16-byte loads): exactly one
-// NVFP4 block, so the block maximum needs no shuffles, and a quad writes 32 contiguous
-// bytes of codes per row.  The E2M1 conversion (cvt.rn.satfinite.e2m1x2) rounds to nearest
-// even and keeps the sign of a negative value that rounds to zero, which is the format rule
-// the codes follow.
+// Work decomposition.  A CTA owns a tile of 128 rows and every nsplit-th 64-column chunk of K
+// (a K split).  At the end each CTA writes its partial down-projection (float32) to
+// the workspace; the last CTA of the row tile to arrive adds the partials in split order
+// (deterministic whatever the arrival order), scales by 1/alpha and writes T in bfloat16.
+// Arrival is counted in one 64-bit word per row tile holding (launch epoch << 8) | count,
+// updated by compare-and-swap: a word left by an earlier launch (finished, aborted, or another
+// layer's use of the same memory) carries another epoch and restarts the count, so the
+// workspace needs no clearing; the last CTA puts the word back to zero, so a replayed launch
+// with the same epoch starts clean as well.
 //
-// Down-projection on the warp MMA (m16n8k16, bf16 in, f32 accumulate).  The registers a
-// thread already holds are used directly as A fragments: the k order inside each 16-wide
-// MMA step is permuted so that thread t's A elements are its own columns
-//   step s: logical k {2t, 2t+1, 2t+8, 2t+9}  <->  chunk columns 16t + 4s + {0, 1, 2, 3},
-// and the B operand (L1 with 1/lambda folded in, prepared at pack time) is stored in the
-// same permuted order ("Lperm": for chunk c, n-tile j, lane l = 4g + t, the 16 values
-// L1'[64c + 16t + i][8j + g], i = 0..15), one 32-byte load per thread and n-tile.
-// With K split over several CTAs, partial sums go to a float32 workspace and the last CTA
-// of a row tile to finish adds them in split order (deterministic), scales by 1/alpha and
-// writes T in bfloat16.
+// Data movement.  The kernel is bound by HBM bandwidth, and each SM's TMA unit takes a copy
+// instruction every few tens of nanoseconds whatever its size, so a stage is two large copies:
+// the 128 x 64 bf16 X tile (one tensor copy, 128-byte swizzle) and the chunk's slice of L1
+// (with 1/lambda folded in, transposed and pre-swizzled at pack time) followed by its 64
+// values of 1/lambda (one bulk copy).
+//
+// Roles (320 threads):
+//   warps 0..7  quantisers: each takes 16 rows of the tile; thread (g = lane/4, t = lane%4)
+//               takes rows g and g+8 and the 16 bf16 at columns 16t..16t+15 of the chunk:
+//               exactly one NVFP4 block, so the block maximum needs no shuffles and a quad
+//               writes 32 contiguous bytes of codes per row
+//   warp 8      TMA producer
+//   warp 9      TMEM owner and MMA issuer: the X tile in shared memory is the A operand of
+//               tcgen05.mma kind::f16 (M = 128, K = 16, bf16), the L1 slice the B operand
+//               (N = rank); T accumulates in TMEM across the CTA's chunks
+// The E2M1 conversion (cvt.rn.satfinite.e2m1x2) rounds to nearest even and keeps the sign of
+// a negative value that rounds to zero, which is the format rule the codes follow.  Block
+// scale code: s8 = E4M3(fl32(amax / fl32(6 s_gX))); one product with the reciprocal lands
+// within one code of it and host-built thresholds (thr[c] = smallest amax whose code is >= c)
+// settle the code exactly; the element scale 1/d comes from a host-built table of
+// fl32(1 / fl32(E4M3value(c) * s_gX)).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -33,236 +47,385 @@ namespace svdq {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kQWarps = 8;                // quantiser warps
+constexpr int kProducer = kQWarps;        // warp 8
+constexpr int kMma = kQWarps + 1;         // warp 9
+constexpr int kThreads = 32 * (kQWarps + 2);
+constexpr int kRows = 128;                // rows per CTA (TMEM lanes)
 constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-template <int NT, int MT>
-__global__ void __launch_bounds__(kWarps * 32) k1_kernel(K1Args a, int chunks_per_split, int nsplit) {
-  constexpr int ROWS = kWarps * 16 * MT;
+struct alignas(64) XMap {
+  unsigned char m[128];
+};
+
+template <int R>   // R = rank (0 or a multiple of 16, <= 128)
+struct Cfg {
+  static constexpr int X_BYTES = kRows * 128;              // 128 rows x 64 bf16
+  static constexpr int L_BYTES = R * 128;                  // R rows x 64 bf16 (L1 slice, transposed)
+  static constexpr int LI_BYTES = L_BYTES + 256;           // + 64 floats of 1/lambda
+  static constexpr int STAGE_BYTES = ((X_BYTES + LI_BYTES + 1023) / 1024) * 1024;
+  static constexpr int STAGES = R > 64 ? 3 : 4;              // two CTAs per SM at every rank
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int RED_BYTES = kRows * (R > 0 ? R : 1) * 4;   // this CTA's partial T
+  static constexpr int SMEM = (RING_BYTES > RED_BYTES ? RING_BYTES : RED_BYTES) + 1024;
+  static constexpr uint32_t TMEM_COLS = R <= 32 ? 32 : (R <= 64 ? 64 : 128);
+  // kind::f16, D f32, A/B bf16, K-major, N = R, M = 128
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(R >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+};
+
+__device__ bool k1_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(err, 4);
+        return false;
+      }
+    }
+  }
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 2)
+    k1_kernel(const __grid_constant__ XMap xmap, K1Args a) {
+  using C = Cfg<R>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], done;
+  __shared__ volatile int abort_flag;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float s_thr[128], s_rcp[128];
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int tile = blockIdx.x, split = blockIdx.y;
   const int64_t M = a.M, K = a.K;
   const int64_t KG = scale_groups(K);
   const int nchunks = int(K / 64);
-  const int c0 = split * chunks_per_split;
-  const int c1 = min(nchunks, c0 + chunks_per_split);
-  const int64_t row_base = int64_t(tile) * ROWS + warp * 16 * MT;
+  const int split = blockIdx.y, nsplit = gridDim.y;
+  // split s takes chunks s, s + nsplit, s + 2 nsplit, ...: the splits of a row tile read
+  // neighbouring column ranges at the same time
+  const int c0 = split;
+  const int64_t row0 = int64_t(blockIdx.x) * kRows;
 
-  float acc[MT][NT > 0 ? NT : 1][4];
-#pragma unroll
-  for (int i = 0; i < MT; ++i)
-#pragma unroll
-    for (int j = 0; j < (NT > 0 ? NT : 1); ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
+  ptx::griddep_launch_dependents();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) (i < 128 ? s_thr[i] : s_rcp[i - 128]) = a.qtab[i];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], kQWarps + (R > 0 ? 1 : 0));
+    }
+    ptx::mbar_init(&done, 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (R > 0 && warp == kMma) {
+    ptx::tmem_alloc(&tmem_slot, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  // every role's bounded waits start once the previous grid is done (the producer first
+  // requests the constant L1 slices, then waits)
+  if (warp != kProducer) ptx::griddep_wait();
 
-  for (int c = c0; c < c1; ++c) {
-    const int64_t col = int64_t(c) * 64 + 16 * t;
-    // raw bf16 of the thread's rows: w[r][0..7], rows r = 2*mt (+g) and 2*mt+1 (+g+8)
-    uint32_t w[2 * MT][8];
-#pragma unroll
-    for (int r = 0; r < 2 * MT; ++r) {
-      const int64_t row = row_base + 16 * (r >> 1) + g + 8 * (r & 1);
-      if (row < M) {
-        const uint16_t* src = a.X + row * K + col;
-        const uint4 u0 = ptx::ld_stream_v4(src);
-        const uint4 u1 = ptx::ld_stream_v4(src + 8);
-        w[r][0] = u0.x; w[r][1] = u0.y; w[r][2] = u0.z; w[r][3] = u0.w;
-        w[r][4] = u1.x; w[r][5] = u1.y; w[r][6] = u1.z; w[r][7] = u1.w;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[r][i] = 0u;
+  if (warp == kProducer) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&xmap);
+      // The L1 / 1/lambda slices are pack-time constants: those of the first ring pass are
+      // requested before waiting for the previous grid (programmatic dependent launch); X,
+      // which that grid may have produced, only after.
+      int pre = 0;
+      for (int c = c0; c < nchunks && pre < C::STAGES; c += nsplit, ++pre) {
+        unsigned char* st = ring + pre * C::STAGE_BYTES;
+        ptx::mbar_arrive_expect_tx(&full[pre], C::X_BYTES + C::LI_BYTES);
+        ptx::bulk_load(st + C::X_BYTES, a.LI + int64_t(c) * C::LI_BYTES, C::LI_BYTES, &full[pre]);
+      }
+      ptx::griddep_wait();
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int c = c0; c < nchunks; c += nsplit, ++issued) {
+        unsigned char* st = ring + stage * C::STAGE_BYTES;
+        if (issued >= pre) {
+          if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err)) break;
+          ptx::mbar_arrive_expect_tx(&full[stage], C::X_BYTES + C::LI_BYTES);
+          ptx::bulk_load(st + C::X_BYTES, a.LI + int64_t(c) * C::LI_BYTES, C::LI_BYTES, &full[stage]);
+        }
+        ptx::tma_load_2d(st, &xmap, &full[stage], 64 * c, int(row0));
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      // every copy issued has landed before shared memory is reused or released
+      for (int i = 0; i < C::STAGES; ++i) {
+        const int used = issued - i;
+        if (used <= 0) continue;
+        const uint32_t last_parity = uint32_t(((used - 1) / C::STAGES) & 1);
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(&full[i], last_parity))
+          if (ptx::globaltimer() - t0 > kTimeoutNs) break;
       }
     }
-    float il[16];
-    {
-      const float4* p = reinterpret_cast<const float4*>(a.inv_lambda + col);
+  } else if (warp == kMma) {
+    // ------------------------------------------------------------ MMA issuer (down-projection)
+    if (R > 0 && lane == 0) {
+      const uint32_t tmem = tmem_slot;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t accumulate = 0;
+      for (int c = c0; c < nchunks; c += nsplit) {
+        if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
+        ptx::tc_fence_after();
+        const uint32_t xs = ptx::smem_u32(ring + stage * C::STAGE_BYTES);
+        const uint32_t ls = xs + C::X_BYTES;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 v = __ldg(p + i);
-        il[4 * i] = v.x; il[4 * i + 1] = v.y; il[4 * i + 2] = v.z; il[4 * i + 3] = v.w;
+        for (int kk = 0; kk < 4; ++kk) {
+          ptx::mma_bf16(tmem, ptx::desc_sw128(xs + 32 * kk), ptx::desc_sw128(ls + 32 * kk), C::IDESC, accumulate);
+          accumulate = 1;
+        }
+        ptx::tc_commit(&empty[stage]);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
       }
+      ptx::tc_commit(&done);
     }
-    // ---- NVFP4 quantisation, two rows at a time (the E4M3 conversions go in pairs)
-#pragma unroll
-    for (int rp = 0; rp < MT; ++rp) {
-      float xh[2][16];
-      float amax[2];
+  } else {
+    // ------------------------------------------------------------ quantiser warps
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int c = c0; c < nchunks; c += nsplit) {
+      if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
+      const unsigned char* st = ring + stage * C::STAGE_BYTES;
+      // raw bf16 of rows g (w[0]) and g + 8 (w[1]) of this warp, columns 16t .. 16t + 15
+      uint32_t w[2][8];
+      float il[16];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int r = 2 * rp + h;
+        const int lr = 16 * warp + g + 8 * h;
+        const unsigned char* rowp = st + lr * 128;
+        const uint4 u0 = *reinterpret_cast<const uint4*>(rowp + (((2 * t) ^ (lr & 7)) << 4));
+        const uint4 u1 = *reinterpret_cast<const uint4*>(rowp + (((2 * t + 1) ^ (lr & 7)) << 4));
+        w[h][0] = u0.x; w[h][1] = u0.y; w[h][2] = u0.z; w[h][3] = u0.w;
+        w[h][4] = u1.x; w[h][5] = u1.y; w[h][6] = u1.z; w[h][7] = u1.w;
+      }
+      {
+        const float4* p = reinterpret_cast<const float4*>(st + C::X_BYTES + C::L_BYTES) + 4 * t;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 v = p[k];
+          il[4 * k] = v.x; il[4 * k + 1] = v.y; il[4 * k + 2] = v.z; il[4 * k + 3] = v.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[stage]);
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+
+      const int64_t col = int64_t(c) * 64 + 16 * t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float2 xh[8];
         float m = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float lo = __uint_as_float(w[r][i] << 16);
-          const float hi = __uint_as_float(w[r][i] & 0xFFFF0000u);
-          xh[h][2 * i] = __fmul_rn(lo, il[2 * i]);
-          xh[h][2 * i + 1] = __fmul_rn(hi, il[2 * i + 1]);
-          m = fmaxf(m, fmaxf(fabsf(xh[h][2 * i]), fabsf(xh[h][2 * i + 1])));
+        for (int k = 0; k < 8; ++k) {
+          const float2 xv = make_float2(__uint_as_float(w[h][k] << 16), __uint_as_float(w[h][k] & 0xFFFF0000u));
+          xh[k] = ptx::mul2_rn(xv, make_float2(il[2 * k], il[2 * k + 1]));
+          m = fmaxf(m, fmaxf(fabsf(xh[k].x), fabsf(xh[k].y)));
         }
-        amax[h] = m;
-      }
-      const float s0 = __fdiv_rn(amax[0], a.six_sgX);
-      const float s1 = __fdiv_rn(amax[1], a.six_sgX);
-      const uint16_t s8 = ptx::cvt_e4m3x2(s1, s0);          // row h=0 in the low byte
-      const float2 dec = ptx::e4m3x2_to_f32x2(s8);
-      uint32_t sc[2] = {uint32_t(s8 & 0xFF), uint32_t(s8 >> 8)};
-      float dd[2] = {dec.x, dec.y};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = 2 * rp + h;
-        const int64_t row = row_base + 16 * rp + g + 8 * h;
+        int code = int(ptx::cvt_e4m3x2(0.f, __fmul_rn(m, a.inv_six)) & 0xFF);
+        code = code - (m < s_thr[code] ? 1 : 0) + (m >= s_thr[code + 1] ? 1 : 0);
+        const uint32_t s8 = uint32_t(code);
+        const int64_t row = row0 + 16 * warp + g + 8 * h;
         uint32_t code0 = 0u, code1 = 0u;
-        if (sc[h] != 0u) {
-          const float d = __fmul_rn(dd[h], a.s_gX);
-          const float rcp = __frcp_rn(d);
-          float q[16];
+        if (s8 != 0u) {
+          const float rcp = s_rcp[code];
+          const float2 r2 = make_float2(rcp, rcp);
+          float2 q[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(xh[h][i], rcp);
-          code0 = ptx::cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-          code1 = ptx::cvt_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
+          for (int k = 0; k < 8; ++k) q[k] = ptx::mul2_rn(xh[k], r2);
+          code0 = ptx::cvt_e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y);
+          code1 = ptx::cvt_e2m1x8(q[4].x, q[4].y, q[5].x, q[5].y, q[6].x, q[6].y, q[7].x, q[7].y);
         }
         if (row < M) {
           uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + col / 2);
           *dst = make_uint2(code0, code1);
         }
         // the quad's four scale bytes of this row form one 32-bit word of the tiled layout
-        uint32_t word = sc[h] << (8 * t);
+        uint32_t word = s8 << (8 * t);
         word |= __shfl_xor_sync(kFull, word, 1);
         word |= __shfl_xor_sync(kFull, word, 2);
-        if (t == ((2 * rp + h) & 3)) {
+        if (t == h) {
           const int64_t off = ((row >> 7) * KG + c) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
           *reinterpret_cast<uint32_t*>(a.x_scales + off) = word;
         }
       }
     }
-    // ---- down-projection: 4 MMA k-steps per chunk
-    if constexpr (NT > 0) {
-      const uint4* lp = reinterpret_cast<const uint4*>(a.Lperm) + (int64_t(c) * NT * 32 + lane) * 2;
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const uint4 b0 = __ldg(lp + j * 64);
-        const uint4 b1 = __ldg(lp + j * 64 + 1);
-        const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            ptx::mma_bf16_16816(acc[mt][j], w[2 * mt][2 * s], w[2 * mt + 1][2 * s], w[2 * mt][2 * s + 1],
-                                w[2 * mt + 1][2 * s + 1], bw[2 * s], bw[2 * s + 1]);
+    // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM
+    if (split == nsplit - 1) {
+      for (int c = nchunks; c < KG; ++c) {
+        const int64_t row = row0 + 16 * warp + g + 8 * t;
+        if (t < 2) {
+          const int64_t off = ((row >> 7) * KG + c) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
+          *reinterpret_cast<uint32_t*>(a.x_scales + off) = 0u;
+        }
       }
     }
   }
 
-  if constexpr (NT > 0) {
-    const int rank = a.rank, r_pad = a.r_pad;
-    const int64_t rows_pad = int64_t(gridDim.x) * ROWS;
-    if (nsplit == 1) {
+  // ---- partial down-projection out; the last CTA of the row tile reduces and stores T
+  if constexpr (R > 0) {
+    __shared__ int s_last;
+    float* part = a.partial + (int64_t(blockIdx.x) * kK1MaxSplit + split) * (R * kRows);
+    if (warp < 4) {
+      // TMEM lane quarter = warp: rows 32 warp + lane; column-major partial, so each store of
+      // one column by the warp is 128 contiguous bytes
+      // a CTA whose K range is empty (more splits than chunks) contributes zeros
+      const bool ok = k1_wait(&done, 0, &abort_flag, a.err) && c0 < nchunks;
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem_slot + (uint32_t(32 * warp) << 16);
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int cb = 0; cb < R; cb += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tbase + cb, v);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t row = row_base + 16 * mt + g + 8 * h;
-          if (row >= M) continue;
-          uint32_t* dst = reinterpret_cast<uint32_t*>(a.T + row * r_pad);
-#pragma unroll
-          for (int j = 0; j < NT; ++j)
-            dst[(8 * j + 2 * t) / 2] = ptx::pack_bf16x2(acc[mt][j][2 * h] * a.inv_alpha,
-                                                         acc[mt][j][2 * h + 1] * a.inv_alpha);
-          for (int j = NT; j < r_pad / 8; ++j) dst[(8 * j + 2 * t) / 2] = 0u;
-        }
-    } else {
-      float* part = a.partial + int64_t(split) * rows_pad * rank;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t row = row_base + 16 * mt + g + 8 * h;
-#pragma unroll
-          for (int j = 0; j < NT; ++j)
-            *reinterpret_cast<float2*>(part + row * rank + 8 * j + 2 * t) =
-                make_float2(acc[mt][j][2 * h], acc[mt][j][2 * h + 1]);
-        }
+        for (int j = 0; j < 32; ++j)
+          if (cb + j < R) part[(cb + j) * kRows + 32 * warp + lane] = ok ? __uint_as_float(v[j]) : 0.f;
+      }
       __threadfence();
-      __syncthreads();
-      __shared__ unsigned int s_last;
-      if (threadIdx.x == 0) s_last = (atomicAdd(a.counters + tile, 1u) == unsigned(nsplit - 1));
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t row = row_base + 16 * mt + g + 8 * h;
-            float sum[NT][2];
-#pragma unroll
-            for (int j = 0; j < NT; ++j) sum[j][0] = sum[j][1] = 0.f;
-            for (int s = 0; s < nsplit; ++s) {
-              const float* ps = a.partial + int64_t(s) * rows_pad * rank + row * rank + 2 * t;
-#pragma unroll
-              for (int j = 0; j < NT; ++j) {
-                const float2 v = __ldcg(reinterpret_cast<const float2*>(ps + 8 * j));
-                sum[j][0] += v.x;
-                sum[j][1] += v.y;
-              }
-            }
-            if (row >= M) continue;
-            uint32_t* dst = reinterpret_cast<uint32_t*>(a.T + row * r_pad);
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-              dst[(8 * j + 2 * t) / 2] = ptx::pack_bf16x2(sum[j][0] * a.inv_alpha, sum[j][1] * a.inv_alpha);
-            for (int j = NT; j < r_pad / 8; ++j) dst[(8 * j + 2 * t) / 2] = 0u;
-          }
-        if (threadIdx.x == 0) a.counters[tile] = 0u;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long* word = a.arrivals + blockIdx.x;
+      const unsigned long long tag = a.epoch << 8;
+      unsigned long long v = atomicAdd(word, 0ull), nv = 0ull;
+      bool swapped = false;
+      for (int it = 0; it < 4096 && !swapped; ++it) {
+        nv = (v >> 8) == a.epoch ? v + 1 : (tag | 1ull);
+        const unsigned long long old = atomicCAS(word, v, nv);
+        swapped = old == v;
+        v = old;
       }
+      if (!swapped) atomicOr(a.err, 8);
+      const bool last = swapped && nv == (tag | unsigned(nsplit));
+      if (last) atomicExch(word, 0ull);
+      s_last = last ? 1 : 0;
+      __threadfence();
+    }
+    __syncthreads();
+    if (s_last) {
+      // one item = 4 rows x 2 columns; every split's float4 of both columns is loaded before
+      // any is added (the adds then run in split order)
+      const float* pt = a.partial + int64_t(blockIdx.x) * kK1MaxSplit * (R * kRows);
+      const int r_pad = a.r_pad;
+      for (int e = threadIdx.x; e < (kRows / 4) * (r_pad / 2); e += blockDim.x) {
+        const int rq = e % (kRows / 4), cp = e / (kRows / 4);
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+        if (2 * cp < R) {
+          float4 p0[kK1MaxSplit], p1[kK1MaxSplit];
+#pragma unroll
+          for (int q = 0; q < kK1MaxSplit; ++q) {
+            if (q < nsplit) {
+              const float4* pq = reinterpret_cast<const float4*>(pt + q * (R * kRows) + (2 * cp) * kRows) + rq;
+              p0[q] = __ldcg(pq);
+              p1[q] = __ldcg(pq + kRows / 4);
+            }
+          }
+          float4 s0 = p0[0], s1 = p1[0];
+#pragma unroll
+          for (int q = 1; q < kK1MaxSplit; ++q) {
+            if (q < nsplit) {
+              s0.x += p0[q].x; s0.y += p0[q].y; s0.z += p0[q].z; s0.w += p0[q].w;
+              s1.x += p1[q].x; s1.y += p1[q].y; s1.z += p1[q].z; s1.w += p1[q].w;
+            }
+          }
+          const float ia = a.inv_alpha;
+          v[0] = ptx::pack_bf16x2(s0.x * ia, s1.x * ia);
+          v[1] = ptx::pack_bf16x2(s0.y * ia, s1.y * ia);
+          v[2] = ptx::pack_bf16x2(s0.z * ia, s1.z * ia);
+          v[3] = ptx::pack_bf16x2(s0.w * ia, s1.w * ia);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int64_t row = row0 + 4 * rq + i;
+          if (row < M) reinterpret_cast<uint32_t*>(a.T + row * r_pad)[cp] = v[i];
+        }
+      }
+    }
+    if (warp == kMma) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc(tmem_slot, C::TMEM_COLS);
     }
   }
 }
 
-template <int NT, int MT>
-int launch_t(const K1Args& a, const K1Plan& p, cudaStream_t s) {
-  dim3 grid(p.row_tiles, p.nsplit);
-  k1_kernel<NT, MT><<<grid, kWarps * 32, 0, s>>>(a, p.chunks_per_split, p.nsplit);
-  return int(cudaGetLastError());
+template <int R>
+int launch_t(const XMap& map, const K1Args& a, const K1Plan& p, cudaStream_t s) {
+  using C = Cfg<R>;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k1_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return int(e);
+    attr_done[dev] = 1;
+  }
+  // programmatic dependent of the previous kernel in the stream: barrier set-up, TMEM
+  // allocation, the tables and the first L1 slices overlap that kernel's drain
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.row_tiles, p.nsplit, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return int(cudaLaunchKernelEx(&cfg, k1_kernel<R>, map, a));
 }
-
-int rows_per_cta(int rank) { return rank > 64 ? kWarps * 16 : kWarps * 32; }
 
 }  // namespace
 
 K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count) {
+  (void)rank;
   K1Plan p;
-  const int rows = rows_per_cta(rank);
-  p.row_tiles = int(ceil_div(M, rows));
+  p.row_tiles = int(ceil_div(M, kRows));
   const int nchunks = int(K / 64);
-  const int target = 3 * sm_count;
-  int nsplit = p.row_tiles > 0 ? int(ceil_div(target, p.row_tiles)) : 1;
-  nsplit = nsplit < 1 ? 1 : (nsplit > nchunks ? nchunks : nsplit);
-  p.chunks_per_split = int(ceil_div(nchunks, nsplit));
-  p.nsplit = int(ceil_div(nchunks, p.chunks_per_split));
+  // K splits per row tile: fill one wave of resident CTAs (two per SM), at most kK1MaxSplit,
+  // at most the chunk count
+  const int slots = 2 * sm_count;
+  int ns = p.row_tiles > 0 ? slots / p.row_tiles : 1;
+  ns = ns < 1 ? 1 : (ns > kK1MaxSplit ? kK1MaxSplit : ns);
+  ns = ns > nchunks ? nchunks : ns;
+  p.nsplit = ns;
+  p.chunks_per_split = int(ceil_div(nchunks, ns));
   return p;
 }
 
-size_t k1_partial_bytes(int64_t M, int64_t K, int rank, int sm_count) {
-  if (rank == 0) return 0;
-  const K1Plan p = k1_plan(M, K, rank, sm_count);
-  if (p.nsplit == 1) return 0;
-  return size_t(p.nsplit) * size_t(p.row_tiles) * size_t(rows_per_cta(rank)) * size_t(rank) * sizeof(float);
+size_t k1_partial_bytes(int64_t M, int rank) {
+  return size_t(ceil_div(M, kRows)) * kK1MaxSplit * kRows * size_t(rank) * sizeof(float);
 }
+size_t k1_arrival_bytes(int64_t M) { return size_t(ceil_div(M, kRows)) * sizeof(unsigned long long); }
 
-int k1_launch(const K1Args& a, const K1Plan& p, void* stream) {
+int k1_launch(const K1Args& a, const K1Plan& p, void* stream, std::string* err) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int nt = a.rank / 8;
-  switch (nt) {
-    case 0: return launch_t<0, 2>(a, p, s);
-    case 2: return launch_t<2, 2>(a, p, s);
-    case 4: return launch_t<4, 2>(a, p, s);
-    case 6: return launch_t<6, 2>(a, p, s);
-    case 8: return launch_t<8, 2>(a, p, s);
-    case 10: return launch_t<10, 1>(a, p, s);
-    case 12: return launch_t<12, 1>(a, p, s);
-    case 14: return launch_t<14, 1>(a, p, s);
-    case 16: return launch_t<16, 1>(a, p, s);
+  XMap map;
+  if (!encode_map_2d(map.m, 2, a.X, uint64_t(a.K), uint64_t(a.M), uint64_t(a.K) * 2, 64, uint32_t(kRows), 1, err))
+    return -1;
+  switch (a.rank) {
+    case 0: return launch_t<0>(map, a, p, s);
+    case 16: return launch_t<16>(map, a, p, s);
+    case 32: return launch_t<32>(map, a, p, s);
+    case 48: return launch_t<48>(map, a, p, s);
+    case 64: return launch_t<64>(map, a, p, s);
+    case 80: return launch_t<80>(map, a, p, s);
+    case 96: return launch_t<96>(map, a, p, s);
+    case 112: return launch_t<112>(map, a, p, s);
+    case 128: return launch_t<128>(map, a, p, s);
     default: return int(cudaErrorInvalidValue);
   }
 }

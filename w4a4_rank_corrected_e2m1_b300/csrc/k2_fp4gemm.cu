@@ -1,7 +1,7 @@
-// Kernel 2: the "dominant 4 bit path" of SVDQuant plus the low-rank up-projection, as one
-// tensor-core GEMM per 256 x 256 output tile (aiflownews article on Nunchaku, "What SVDQuant
-// actually does": a compact high-precision low-rank path and a 4-bit path whose results are
-// summed; Nunchaku section: the two branches share outputs).
+// Kernel 2: the 4-bit branch of SVDQuant, which carries most of the arithmetic, plus the
+// low-rank up-projection, as one tensor-core GEMM per 256 x 256 output tile.  The layer's
+// output is the sum of the two branches (aiflownews article on Nunchaku, "What SVDQuant
+// actually does"), and the Nunchaku section fuses them so the output is written once.
 //
 //   acc  = sum_k  sX * sW * e2m1(x) * e2m1(w)      tcgen05.mma kind::mxf4nvf4, UE4M3 scales
 //                                                  per 16 K (scale_vec::4X), E2M1 operands
@@ -172,6 +172,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int iters = n_lr + n_k;
   const int64_t KG = scale_groups(K);
 
+  ptx::griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(&s->full[i], 1);
@@ -203,10 +204,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   ptx::cluster_sync();                            // barriers of both CTAs initialised, TMEM allocated
   ptx::tc_fence_after();
   const uint32_t tmem = s->tmem_base;
+  // every role's bounded waits start once the previous grid is done (the producer first
+  // issues the weight loads of its first ring pass, then waits)
+  if (warp != 0) ptx::griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
+      // Weight-side loads (L2, R codes and scales) depend on nothing kernel 1 writes: those of
+      // the first tile's first ring pass are issued before waiting for the previous grid, so
+      // they overlap its tail when this grid is launched as its programmatic dependent.
+      const int pre = pair < num_tiles ? (iters < STAGES ? iters : STAGES) : 0;
+      auto weight_loads = [&](int it, int n0, int nb, unsigned char* st, uint64_t* fb) {
+        if (it < n_lr) {
+          ptx::mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+          ptx::tma_load_2d(st + A_BYTES, &maps.L2, fb, 64 * it, nb);
+        } else {
+          const int kq = it - n_lr;
+          ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          ptx::tma_load_2d(st + A_BYTES, &maps.B, fb, 128 * kq, nb);
+          // scales: 2 KB chunks = 8 rows of the 256-byte-wide view of the tiled buffers
+          unsigned char* sfb = st + A_BYTES + B_BYTES + SFA_BYTES;
+          ptx::tma_load_2d(sfb, &maps.SFB, fb, 0, int(((int64_t(n0) / 128) * KG + 4 * kq) * 2));
+          ptx::tma_load_2d(sfb + SFA_BYTES, &maps.SFB, fb, 0, int(((int64_t(n0) / 128 + 1) * KG + 4 * kq) * 2));
+        }
+      };
+      auto act_loads = [&](int it, int m0, unsigned char* st, uint64_t* fb) {
+        if (it < n_lr) {
+          ptx::tma_load_2d(st, &maps.T, fb, 64 * it, m0);
+        } else {
+          const int kq = it - n_lr;
+          ptx::tma_load_2d(st, &maps.A, fb, 128 * kq, m0);
+          ptx::tma_load_2d(st + A_BYTES + B_BYTES, &maps.SFA, fb, 0, int(((int64_t(m0) / 128) * KG + 4 * kq) * 2));
+        }
+      };
+      if (pre > 0) {
+        const int n0 = (pair % num_n) * BN;
+        for (int it = 0; it < pre; ++it)   // stages start empty: no wait
+          weight_loads(it, n0, n0 + int(rank) * (BN / 2), stages + it * STAGE_BYTES, &s->full[it]);
+      }
+      ptx::griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -215,24 +252,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int n0 = (tile % num_n) * BN;
         const int nb = n0 + int(rank) * (BN / 2);   // this CTA's half of the weight rows
         for (int it = 0; it < iters; ++it) {
-          if (!wait_bounded(&s->empty[stage], phase ^ 1u, s, a.err)) { ok = false; break; }
           unsigned char* st = stages + stage * STAGE_BYTES;
           uint64_t* fb = &s->full[stage];
-          if (it < n_lr) {
-            ptx::mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-            ptx::tma_load_2d(st, &maps.T, fb, 64 * it, m0);
-            ptx::tma_load_2d(st + A_BYTES, &maps.L2, fb, 64 * it, nb);
-          } else {
-            const int kq = it - n_lr;
-            ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            ptx::tma_load_2d(st, &maps.A, fb, 128 * kq, m0);
-            ptx::tma_load_2d(st + A_BYTES, &maps.B, fb, 128 * kq, nb);
-            // scales: 2 KB chunks = 8 rows of the 256-byte-wide view of the tiled buffers
-            ptx::tma_load_2d(st + A_BYTES + B_BYTES, &maps.SFA, fb, 0, int(((int64_t(m0) / 128) * KG + 4 * kq) * 2));
-            unsigned char* sfb = st + A_BYTES + B_BYTES + SFA_BYTES;
-            ptx::tma_load_2d(sfb, &maps.SFB, fb, 0, int(((int64_t(n0) / 128) * KG + 4 * kq) * 2));
-            ptx::tma_load_2d(sfb + SFA_BYTES, &maps.SFB, fb, 0, int(((int64_t(n0) / 128 + 1) * KG + 4 * kq) * 2));
+          if (!(tile == pair && it < pre)) {
+            if (!wait_bounded(&s->empty[stage], phase ^ 1u, s, a.err)) { ok = false; break; }
+            weight_loads(it, n0, nb, st, fb);
           }
+          act_loads(it, m0, st, fb);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -415,8 +441,19 @@ int k2_launch(const K2Maps& maps, const K2Args& a, int sm_count, void* stream) {
     max_pairs[dev] = n;
   }
   const int pairs = int(tiles < max_pairs[dev] ? tiles : max_pairs[dev]);
-  k2_kernel<<<2 * pairs, THREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(maps, a);
-  return int(cudaGetLastError());
+  // launched as a programmatic dependent of the previous kernel in the stream: the prologue
+  // and the first weight loads run while that kernel drains (only the TMA producer waits on it)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return int(cudaLaunchKernelEx(&cfg, k2_kernel, maps, a));
 }
 
 }  // namespace svdq

@@ -15,6 +15,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <limits>
 #include <new>
 
 #include "svdq_internal.h"
@@ -114,6 +115,31 @@ static void quantize_row(const float* v, int64_t K, float s_g, uint8_t* codes, u
       const uint8_t hi = e2m1_encode(x[2 * i + 1] * rcp);
       c[i] = uint8_t(lo | (hi << 4));
     }
+  }
+}
+
+void act_quant_tables(float s_g, float* thr, float* rcp) {
+  const float six = 6.0f * s_g;
+  auto code_of = [&](uint32_t bits) {
+    float a;
+    std::memcpy(&a, &bits, 4);
+    return int(e4m3_encode_nonneg(a / six));
+  };
+  thr[0] = 0.f;
+  for (int c = 1; c < 127; ++c) {
+    uint32_t lo = 0, hi = 0x7F800000u;              // +inf saturates to the top code
+    while (lo < hi) {                               // smallest bit pattern whose code is >= c
+      const uint32_t mid = lo + (hi - lo) / 2;
+      if (code_of(mid) >= c) hi = mid;
+      else lo = mid + 1;
+    }
+    std::memcpy(&thr[c], &lo, 4);
+  }
+  thr[127] = std::numeric_limits<float>::infinity();
+  rcp[0] = 0.f;
+  for (int c = 1; c < 128; ++c) {
+    const float d = e4m3_decode(uint8_t(c)) * s_g;
+    rcp[c] = 1.0f / d;
   }
 }
 

@@ -31,6 +31,13 @@ struct HostPack {
 // Validates p and runs smoothing, SVD, residual and NVFP4 quantisation on the CPU.
 svdq_status_t pack_on_host(const svdq_pack_params_t* p, HostPack* out, std::string* err);
 
+// Activation-quantiser tables for a global scale s_g (host side):
+//   thr[c]  smallest float32 amax >= 0 whose block scale E4M3(fl32(amax / fl32(6 s_g))) >= c
+//           (c = 0..126; thr[127] = +inf), so the scale code of a block is the number of
+//           thresholds <= amax;
+//   rcp[c]  fl32(1 / fl32(E4M3value(c) * s_g)) (rcp[0] = 0, unused).
+void act_quant_tables(float s_g, float* thr128, float* rcp128);
+
 // Format helpers (host side).
 float bf16_to_f32(uint16_t b);
 uint16_t f64_to_bf16(double a);
@@ -47,24 +54,30 @@ SVDQ_HD inline int64_t rank_pad(int64_t r) { return r == 0 ? 0 : round_up(r, 64)
 
 // ------------------------------------------------------------------ kernel 1 (k1_actquant.cu)
 struct K1Args {
-  const uint16_t* X;          // M x K bf16
-  const float* inv_lambda;    // K
-  const uint16_t* Lperm;      // folded + permuted L1 (see k1_actquant.cu), may be null if rank == 0
+  const uint16_t* X;          // M x K bf16 (read through the tensor map passed beside these args)
+  const unsigned char* LI;    // per 64-column chunk: swizzled L1' slice (rank x 128 B) then 1/lambda (256 B)
   uint8_t* x_codes;           // M x K/2
   uint8_t* x_scales;          // tiled
   uint16_t* T;                // M x r_pad bf16 (null if rank == 0)
-  float* partial;             // split-K partial sums [nsplit][M_pad128][rank] fp32
-  unsigned int* counters;     // one per 128-row tile, zero between calls
+  float* partial;             // split-K partial sums [row tile][split][rank][128] (rank > 0)
+  unsigned long long* arrivals;   // one word per row tile: (epoch << 8) | CTAs arrived
+  unsigned long long epoch;   // unique per launch, < 2^56
   int64_t M, K;
   int rank, r_pad;
-  float s_gX, six_sgX, inv_alpha;
+  float s_gX, inv_six, inv_alpha;
+  const float* qtab;          // 256 floats: E4M3 scale thresholds [0,128), reciprocals [128,256)
+  int* err;                   // device error word (bounded waits)
 };
 struct K1Plan {
   int row_tiles = 0, nsplit = 1, chunks_per_split = 1;
 };
 K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count);
-size_t k1_partial_bytes(int64_t M, int64_t K, int rank, int sm_count);
-int k1_launch(const K1Args& a, const K1Plan& plan, void* stream);  // returns cudaError_t
+constexpr int kK1MaxSplit = 8;   // K splits per 128-row tile
+// Workspace bytes of the split-K partial sums and the arrival words for M rows.
+size_t k1_partial_bytes(int64_t M, int rank);
+size_t k1_arrival_bytes(int64_t M);
+// Encodes the tensor map of X and launches; returns a cudaError_t (or -1 if the map failed).
+int k1_launch(const K1Args& a, const K1Plan& plan, void* stream, std::string* err);
 
 // ------------------------------------------------------------------ kernel 2 (k2_fp4gemm.cu)
 struct K2Maps {
