@@ -34,6 +34,31 @@ from w4a4_rank_corrected_e2m1_b300 import synthetic  # noqa: E402
 METRIC = "fused SVDQuant W4A4 linear TFLOPS & tokens/s at FLUX shapes; % of FP4 roofline"
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on B300
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from the ncu
+# captures summarised under profiles/, keyed by the workload and by a hash of the kernel's
+# sources at capture time: a kernel edited since then reports null traffic.
+NCU_TRAFFIC = {
+    ("flux_mlp_up", "k1_actquant"): ("bf09ba97012e1cec", 28.549632e6 + 0.025344e6),
+    ("flux_mlp_up", "k2_fp4gemm"): ("594f6e9e8c533bfc", 33.080064e6 + 63.747072e6),
+}
+KERNEL_SOURCES = {
+    "k1_actquant": ["k1_actquant.cu", "ptx.cuh", "svdq_internal.h"],
+    "k2_fp4gemm": ["k2_fp4gemm.cu", "ptx.cuh", "svdq_internal.h"],
+}
+
+
+def ncu_traffic(workload, kernel):
+    """Captured DRAM bytes per launch, or None if absent or the kernel changed since."""
+    import hashlib
+    entry = NCU_TRAFFIC.get((workload, kernel))
+    if entry is None:
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "w4a4_rank_corrected_e2m1_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return entry[1] if h.hexdigest()[:16] == entry[0] else None
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -52,6 +77,28 @@ def peaks():
         d = json.load(open(path))
         return d["hbm_gbs"], d["bf16_tflops"], "measured"
     return 6400.0, 1800.0, "fallback"
+
+
+def batch_seeds(rank, nbuf):
+    """Seeds of the activation batches a rank cycles through: disjoint across ranks, so the
+    replicas work on different tokens."""
+    return [1000 * rank + i for i in range(nbuf)]
+
+
+def max_over_ranks(values, world, device):
+    """Element-wise maximum over ranks of per-rank floats: the job's time is its slowest rank's."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_rate(units_per_rank, world, seconds):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / seconds
 
 
 def workload_flops(w, rows=None):
@@ -247,7 +294,7 @@ def run_ours(args, w):
 
     # distinct activation batches per step (rank-specific seeds), resident in HBM
     nbuf = 4
-    Xs = [torch.from_numpy(synthetic.make_x(w, M, seed=1000 * rank + i).view(np.int16)).cuda() for i in range(nbuf)]
+    Xs = [torch.from_numpy(synthetic.make_x(w, M, seed=sd).view(np.int16)).cuda() for sd in batch_seeds(rank, nbuf)]
     Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
@@ -312,19 +359,13 @@ def run_ours(args, w):
     barrier()
 
     # max over ranks
-    ms_step = sum(fwd_ms) / len(fwd_ms)
-    if world > 1:
-        tt = torch.tensor([ms_step, statistics.median(e2e_t)], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step, e2e_med = float(tt[0]), float(tt[1])
-    else:
-        e2e_med = statistics.median(e2e_t)
+    ms_step, e2e_med = max_over_ranks([sum(fwd_ms) / len(fwd_ms), statistics.median(e2e_t)], world, "cuda")
 
     if rank == 0:
         hbm, bf16, src = peaks()
         fp4_peak = bf16 * FP4_OVER_BF16
         flops = workload_flops(w)
-        tflops = flops * world / (ms_step * 1e-3) / 1e12
+        tflops = job_rate(flops, world, ms_step * 1e-3) / 1e12
         k2_fp4_flops = 2.0 * M * N * K
         k2_achieved = k2_fp4_flops / (t_k2 * 1e-3) / 1e12
         k1_bytes = M * K * 2 + M * K // 2 + M * K // 16 + M * w.rank * 2 + K * w.rank * 2 + K * 4
@@ -336,17 +377,20 @@ def run_ours(args, w):
             "config": {"workload": w.name, "M": M, "K": K, "N": N, "rank": w.rank, "per_gpu_tokens": M,
                        "l2": "flushed before every timed step (256 MiB write outside the timed events)",
                        "parallelism": f"replicas x{world} (token shards, no collective)"},
-            "tokens_per_s": M * world / (ms_step * 1e-3),
+            "tokens_per_s": job_rate(M, world, ms_step * 1e-3),
             "kernels_ms": {"k1_actquant": t_k1, "k2_fp4gemm": t_k2},
             "roofline": {"bound": "tensor", "kernel": "k2_fp4gemm", "achieved": k2_achieved, "peak": fp4_peak,
-                         "unit": "TFLOP/s", "frac": k2_achieved / fp4_peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": k2_achieved / fp4_peak,
+                         "traffic": ncu_traffic(w.name, "k2_fp4gemm"), "traffic_unit": "bytes per launch (ncu)",
+                         "algorithmic_flop": k2_fp4_flops,
                          "peak_source": f"{src} bf16 {bf16} TFLOP/s x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
             "roofline_k1": {"bound": "hbm", "kernel": "k1_actquant", "achieved": k1_bytes / (t_k1 * 1e-3) / 1e9,
                             "peak": hbm, "unit": "GB/s", "frac": k1_bytes / (t_k1 * 1e-3) / 1e9 / hbm,
-                            "traffic": None},
+                            "traffic": ncu_traffic(w.name, "k1_actquant"), "traffic_unit": "bytes per launch (ncu)",
+                            "algorithmic_bytes": k1_bytes},
             "lowrank": {"rank": w.rank, "fwd_ms": ms_step, "fwd_rank0_ms": r0_step,
                         "added_frac_of_4bit_gemm": (ms_step - r0_step) / t_k2},
-            "e2e": {"value": flops * world / e2e_med / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": job_rate(flops, world, e2e_med) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
                     "ms_per_step": e2e_med * 1e3},
             "gpu_launches": 2 * args.steps,
