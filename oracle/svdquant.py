@@ -176,6 +176,20 @@ def forward(X_bits, p, rows=None):
     return Y + bf16_to_f64(p["bias"])[None, :]
 
 
+def lora_delta(X_bits, A_bits, B_bits, scale, rows=None):
+    """The LoRA adapter's contribution scale * (X A) B in float64, X in bf16 values.
+
+    The pages note that SVDQuant keeps working with existing LoRA adapters without
+    re-quantising the residual (aiflownews article on Nunchaku, "What SVDQuant actually
+    does"), i.e. the adapter is a further 16-bit branch beside the low-rank one; it acts on
+    the layer's input X, which is what the adapter was trained against.
+    """
+    Xb = np.asarray(X_bits)
+    if rows is not None:
+        Xb = Xb[rows]
+    return float(scale) * ((bf16_to_f64(Xb) @ bf16_to_f64(A_bits)) @ bf16_to_f64(B_bits))
+
+
 def forward_cols(X_bits, p, rows, cols):
     """Sampled outputs Y[rows][:, cols] (same arithmetic as forward, fewer weight rows)."""
     sub = dict(p)

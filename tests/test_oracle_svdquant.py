@@ -146,3 +146,47 @@ def test_residual_against_rounded_factors(tiny):
     assert np.array_equal(p["R"], (Wh - LL.T).astype(np.float32))
     # the rank-r branch carries the spike: the residual is much smaller than W^
     assert np.linalg.norm(p["R"]) < 0.8 * np.linalg.norm(Wh)
+
+
+# ------------------------------------------------------------------ LoRA term
+def _lora_case(seed, M=6, K=16, N=12, r=3):
+    rng = np.random.default_rng(seed)
+    X = sq.f64_to_bf16(rng.standard_normal((M, K)))
+    A = sq.f64_to_bf16(rng.standard_normal((K, r)))
+    B = sq.f64_to_bf16(rng.standard_normal((r, N)))
+    return X, A, B
+
+
+def test_lora_delta_against_python_loops():
+    """Brute force on a tiny case: sum_j sum_k x_ik a_kj b_jn, written as loops."""
+    X, A, B = _lora_case(11)
+    x, a, b = sq.bf16_to_f64(X), sq.bf16_to_f64(A), sq.bf16_to_f64(B)
+    M, K = x.shape
+    r, N = b.shape
+    ref = np.zeros((M, N))
+    for i in range(M):
+        for n in range(N):
+            acc = 0.0
+            for j in range(r):
+                t = 0.0
+                for k in range(K):
+                    t += x[i, k] * a[k, j]
+                acc += t * b[j, n]
+            ref[i, n] = 0.75 * acc
+    got = sq.lora_delta(X, A, B, 0.75)
+    assert np.allclose(got, ref, rtol=1e-13, atol=1e-12)
+
+
+def test_lora_delta_zero_and_linear_in_scale():
+    X, A, B = _lora_case(12)
+    assert np.all(sq.lora_delta(X, A, np.zeros_like(B), 3.0) == 0.0)
+    assert np.all(sq.lora_delta(X, A, B, 0.0) == 0.0)
+    d1 = sq.lora_delta(X, A, B, 1.0)
+    assert np.allclose(sq.lora_delta(X, A, B, -2.5), -2.5 * d1, rtol=1e-14, atol=1e-14)
+
+
+def test_lora_delta_rows_subset_matches_full():
+    X, A, B = _lora_case(13, M=9)
+    full = sq.lora_delta(X, A, B, 0.5)
+    rows = np.array([0, 4, 8])
+    assert np.array_equal(sq.lora_delta(X, A, B, 0.5, rows=rows), full[rows])
