@@ -109,7 +109,7 @@ typedef struct {
 } svdq_packed_host_t;
 
 typedef struct {
-  int64_t N, K, rank, r_pad, M_max;
+  int64_t N, K, rank, lora_rank, r_pad, M_max;   /* r_pad: T width, 64 * ceil((rank + lora_rank) / 64) */
   float s_gW, s_gX, alpha;
   int32_t device, sm_count;
 } svdq_info_t;
@@ -140,6 +140,24 @@ svdq_status_t svdq_get_info(svdq_handle_t h, svdq_info_t* info);
 
 /* Copy of the packed layer in canonical host layouts (see svdq_packed_host_t). */
 svdq_status_t svdq_export(svdq_handle_t h, svdq_packed_host_t* out);
+
+/*
+ * svdq_attach_lora -- appends a LoRA adapter to the 16-bit low-rank branch without touching
+ * the quantised residual: the forward becomes Y = (SVDQuant layer) + scale * (X A) B.  The
+ * pages note that SVDQuant works with existing LoRA adapters without re-quantisation
+ * (aiflownews article on Nunchaku, "What SVDQuant actually does"); here the adapter's factors
+ * are concatenated onto L1 and L2, so the kernels run with rank + r_lora and the up- and
+ * down-projections of both share the same passes.
+ *   A_bf16  host, K x r_lora row-major (bf16 bits); the library keeps bf16(scale * A)
+ *   B_bf16  host, r_lora x N row-major (bf16 bits)
+ *   r_lora  multiple of 16 with rank + r_lora <= 128; 0 removes the adapter (A, B may be NULL)
+ * Synchronises the handle's device, then replaces the handle's low-rank buffers; the layer's
+ * own workspace grows if needed, a lent one must already be large enough (else
+ * SVDQ_ERR_WORKSPACE and the layer is unchanged).  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
+ * WORKSPACE, OOM, CUDA.  svdq_export keeps returning the SVD factors alone.
+ */
+svdq_status_t svdq_attach_lora(svdq_handle_t h, const uint16_t* A_bf16, const uint16_t* B_bf16, int64_t r_lora,
+                               float scale, void* stream);
 
 /* Bytes of the activation-scale buffer for M rows (tiled layout above). */
 int64_t svdq_scales_bytes(int64_t M, int64_t K);

@@ -110,6 +110,12 @@ struct svdq_layer {
   uint16_t* d_bias = nullptr;
   int* d_err = nullptr;
   K2Maps maps{};                   // B and L2 filled at pack
+  // LoRA factors appended to the low-rank branch (svdq_attach_lora): r_lora columns of
+  // bf16(scale * A) after L1's columns, r_lora rows of B after L2's rows
+  int64_t r_lora = 0;
+  std::vector<uint16_t> lora_A;    // K x r_lora (bf16 bits, scale applied)
+  std::vector<uint16_t> lora_B;    // r_lora x N (bf16 bits)
+  int64_t rank_k() const { return host.rank + r_lora; }   // rank the kernels run with
   // workspace
   unsigned char* ws = nullptr;
   size_t ws_bytes = 0;
@@ -127,7 +133,7 @@ struct WsLayout {
 
 WsLayout ws_layout(const svdq_layer* h, int64_t M, bool staging) {
   WsLayout w{};
-  const int64_t K = h->host.K, N = h->host.N, r = h->host.rank;
+  const int64_t K = h->host.K, N = h->host.N, r = h->rank_k();
   size_t off = 0;
   w.codes = off; off += align256(size_t(M) * K / 2);
   w.scales = off; off += align256(size_t(svdq_scales_bytes(M, K)));
@@ -169,6 +175,66 @@ void free_layer(svdq_layer* h) {
   if (h->ws_owned) cudaFree(h->ws);
 }
 
+// Device layouts of the low-rank branch for the handle's kernel rank (SVD rank plus any LoRA
+// rank), uploaded into fresh buffers that replace the old ones:
+//   LI   per 64-column chunk c: the chunk's slice of L1' (rank_k rows of 64 K-values, bf16,
+//        K-major, 128-byte rows with the 128-byte swizzle the tensor cores read: 16-byte unit u
+//        of row j stored at unit u ^ (j % 8)), then the chunk's 64 values of 1/lambda (fp32).
+//        L1' = diag(1/lambda) L1 for the SVD columns (kernel 1 multiplies raw X by it, which
+//        is X^ L1), and bf16(scale * A) for the LoRA columns (X A needs no smoothing)
+//   L2t  N x r_pad bf16: L2 transposed, then B transposed, zero padding
+svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
+  const HostPack& hp = h->host;
+  const int64_t N = hp.N, K = hp.K, r = hp.rank, rl = h->r_lora, rk = r + rl;
+  const int64_t r_pad = rank_pad(rk);
+  std::vector<uint16_t> l2t(size_t(N) * std::max<int64_t>(r_pad, 1), 0);
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t j = 0; j < r; ++j) l2t[n * r_pad + j] = hp.L2[j * N + n];
+    for (int64_t j = 0; j < rl; ++j) l2t[n * r_pad + r + j] = h->lora_B[j * N + n];
+  }
+  const int64_t li_chunk = rk * 128 + 256;
+  std::vector<unsigned char> li(size_t(K / 64) * li_chunk, 0);
+  for (int64_t c = 0; c < K / 64; ++c) {
+    unsigned char* base = li.data() + c * li_chunk;
+    for (int64_t j = 0; j < rk; ++j)
+      for (int i = 0; i < 64; ++i) {
+        const int64_t k = 64 * c + i;
+        const uint16_t v = j < r ? f64_to_bf16(double(hp.inv_lambda[k]) * double(bf16_to_f32(hp.L1[k * r + j])))
+                                 : h->lora_A[k * rl + (j - r)];
+        const int unit = (i / 8) ^ int(j % 8);
+        reinterpret_cast<uint16_t*>(base + j * 128 + unit * 16)[i % 8] = v;
+      }
+    std::memcpy(base + rk * 128, hp.inv_lambda.data() + 64 * c, 256);
+  }
+  cudaError_t e;
+  uint16_t* d_l2t = static_cast<uint16_t*>(dalloc(l2t.size() * 2, &e));
+  unsigned char* d_li = nullptr;
+  if (e == cudaSuccess) d_li = static_cast<unsigned char*>(dalloc(li.size(), &e));
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_l2t, l2t.data(), l2t.size() * 2, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_li, li.data(), li.size(), cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  K2Maps maps = h->maps;
+  std::string err;
+  if (e == cudaSuccess && rk > 0 && !encode_map_2d(maps.L2, 2, d_l2t, r_pad, N, r_pad * 2, 64, 128, 1, &err)) {
+    cudaFree(d_l2t);
+    cudaFree(d_li);
+    return fail(SVDQ_ERR_CUDA, err);
+  }
+  if (e != cudaSuccess) {
+    cudaFree(d_l2t);
+    cudaFree(d_li);
+    return e == cudaErrorMemoryAllocation ? fail(SVDQ_ERR_OOM, "device allocation failed")
+                                          : cuda_fail(e, "uploading the low-rank branch");
+  }
+  cudaFree(h->d_L2t);
+  cudaFree(h->d_LI);
+  h->d_L2t = d_l2t;
+  h->d_LI = d_li;
+  h->maps = maps;
+  h->r_pad = r_pad;
+  return SVDQ_OK;
+}
+
 svdq_status_t attach_workspace(svdq_layer* h, void* ptr, size_t bytes, int64_t M_max, bool staging, bool owned,
                                cudaStream_t stream) {
   if (h->ws_owned && h->ws) cudaFree(h->ws);
@@ -201,7 +267,7 @@ svdq_status_t launch_k1(svdq_layer* h, const void* X, int64_t M, void* codes, vo
   a.T = static_cast<uint16_t*>(T);
   a.M = M;
   a.K = h->host.K;
-  a.rank = int(h->host.rank);
+  a.rank = int(h->rank_k());
   a.r_pad = int(h->r_pad);
   a.s_gX = h->host.s_gX;
   a.inv_six = h->inv_six;
@@ -225,7 +291,7 @@ svdq_status_t launch_k2(svdq_layer* h, const void* codes, const void* scales, co
       !encode_map_2d(maps.SFA, 1, scales, 256, svdq_scales_bytes(M, K) / 256, 256, 256, 8, 0, &err) ||
       !encode_map_2d(maps.Y, 2, Y, N, M, N * 2, 64, 32, 1, &err))
     return fail(SVDQ_ERR_CUDA, err);
-  if (h->host.rank > 0 && !encode_map_2d(maps.T, 2, T, h->r_pad, M, h->r_pad * 2, 64, 128, 1, &err))
+  if (h->rank_k() > 0 && !encode_map_2d(maps.T, 2, T, h->r_pad, M, h->r_pad * 2, 64, 128, 1, &err))
     return fail(SVDQ_ERR_CUDA, err);
   K2Args a{};
   a.bias = h->d_bias;
@@ -233,7 +299,7 @@ svdq_status_t launch_k2(svdq_layer* h, const void* codes, const void* scales, co
   a.M = M;
   a.N = N;
   a.K = K;
-  a.rank = int(h->host.rank);
+  a.rank = int(h->rank_k());
   a.alpha = h->host.alpha;
   const int e = k2_launch(maps, a, h->sm_count, stream);
   if (e != 0) return cuda_fail(cudaError_t(e), "kernel 2 launch");
@@ -312,8 +378,7 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
   cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
   h->device = p->device;
   cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, p->device);
-  const int64_t N = p->N, K = p->K, r = p->rank;
-  h->r_pad = rank_pad(r);
+  const int64_t N = p->N, K = p->K;
   const HostPack& hp = h->host;
   h->inv_six = 1.0f / (6.0f * hp.s_gX);
   h->inv_alpha = 1.0f / hp.alpha;
@@ -328,28 +393,6 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
     for (int64_t j = 0; j < K / 16; ++j)
       sc_tiled[((n / 128) * KG + j / 4) * 512 + (n % 32) * 16 + ((n % 128) / 32) * 4 + (j % 4)] =
           hp.R_scales[n * (K / 16) + j];
-  std::vector<uint16_t> l2t(size_t(N) * std::max<int64_t>(h->r_pad, 1), 0);
-  for (int64_t n = 0; n < N; ++n)
-    for (int64_t j = 0; j < r; ++j) l2t[n * h->r_pad + j] = hp.L2[j * N + n];
-  // per 64-column chunk c: L1' = diag(1/lambda) L1 in bf16, transposed to rank rows of 64
-  // K-values (128 bytes, K-major) and laid out with the 128-byte swizzle the tensor cores read
-  // (16-byte unit u of row j stored at unit u ^ (j % 8)), followed by the chunk's 64 values of
-  // 1/lambda as float32
-  const int64_t l_bytes = r * 128;
-  const int64_t li_chunk = l_bytes + 256;
-  std::vector<unsigned char> li(size_t(K / 64) * li_chunk, 0);
-  for (int64_t c = 0; c < K / 64; ++c) {
-    unsigned char* base = li.data() + c * li_chunk;
-    for (int64_t j = 0; j < r; ++j)
-      for (int i = 0; i < 64; ++i) {
-        const int64_t k = 64 * c + i;
-        const double v = double(hp.inv_lambda[k]) * double(bf16_to_f32(hp.L1[k * r + j]));
-        const int unit = (i / 8) ^ int(j % 8);
-        reinterpret_cast<uint16_t*>(base + j * 128 + unit * 16)[i % 8] = f64_to_bf16(v);
-      }
-    std::memcpy(base + l_bytes, hp.inv_lambda.data() + 64 * c, 256);
-  }
-
   // ---- upload
   auto up = [&](void** dst, const void* src, size_t bytes) -> cudaError_t {
     cudaError_t ee;
@@ -360,8 +403,6 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
   };
   e = up(reinterpret_cast<void**>(&h->d_R_codes), hp.R_codes.data(), hp.R_codes.size());
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_R_scales), sc_tiled.data(), sc_tiled.size());
-  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_L2t), l2t.data(), l2t.size() * 2);
-  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_LI), li.data(), li.size());
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_inv_lambda), hp.inv_lambda.data(), K * 4);
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_qtab), qtab.data(), qtab.size() * 4);
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_bias), hp.bias.data(), N * 2);
@@ -377,11 +418,16 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
                                           : cuda_fail(e, "uploading the packed layer");
   }
   if (!encode_map_2d(h->maps.B, 1, h->d_R_codes, K / 2, N, K / 2, 128, 128, 1, &err) ||
-      !encode_map_2d(h->maps.SFB, 1, h->d_R_scales, 256, int64_t(sc_tiled.size()) / 256, 256, 256, 8, 0, &err) ||
-      (r > 0 && !encode_map_2d(h->maps.L2, 2, h->d_L2t, h->r_pad, N, h->r_pad * 2, 64, 128, 1, &err))) {
+      !encode_map_2d(h->maps.SFB, 1, h->d_R_scales, 256, int64_t(sc_tiled.size()) / 256, 256, 256, 8, 0, &err)) {
     free_layer(h);
     delete h;
     return fail(SVDQ_ERR_CUDA, err);
+  }
+  s = upload_low_rank(h, stream);
+  if (s != SVDQ_OK) {
+    free_layer(h);
+    delete h;
+    return s;
   }
   if (p->M_max > 0) {
     s = svdq_reserve(h, p->M_max, 0);
@@ -409,6 +455,7 @@ svdq_status_t svdq_get_info(svdq_handle_t h, svdq_info_t* info) {
   info->N = h->host.N;
   info->K = h->host.K;
   info->rank = h->host.rank;
+  info->lora_rank = h->r_lora;
   info->r_pad = h->r_pad;
   info->M_max = h->ws_M;
   info->s_gW = h->host.s_gW;
@@ -442,6 +489,45 @@ svdq_status_t svdq_workspace_size(svdq_handle_t h, int64_t M, int32_t host_stagi
   return SVDQ_OK;
 }
 
+svdq_status_t svdq_attach_lora(svdq_handle_t h, const uint16_t* A_bf16, const uint16_t* B_bf16, int64_t r_lora,
+                               float scale, void* stream) {
+  if (!h || r_lora < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative LoRA rank");
+  if (r_lora > 0 && (!A_bf16 || !B_bf16)) return fail(SVDQ_ERR_INVALID_ARG, "null LoRA factor");
+  if (!std::isfinite(scale)) return fail(SVDQ_ERR_INVALID_ARG, "LoRA scale must be finite");
+  const int64_t K = h->host.K, N = h->host.N, rk = h->host.rank + r_lora;
+  if (r_lora % 16 != 0 || rk > 128)
+    return fail(SVDQ_ERR_UNSUPPORTED_SHAPE, "LoRA rank must be a multiple of 16 with rank + LoRA rank <= 128");
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaDeviceSynchronize();                 // no kernel still reads the old buffers
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronisation");
+  std::vector<uint16_t> A(size_t(K) * r_lora), B(B_bf16 ? B_bf16 : nullptr, B_bf16 ? B_bf16 + size_t(r_lora) * N : nullptr);
+  for (size_t i = 0; i < A.size(); ++i) A[i] = f64_to_bf16(double(scale) * double(bf16_to_f32(A_bf16[i])));
+  // the workspace layout depends on the kernel rank: a lent workspace must already be big enough
+  const int64_t old_rl = h->r_lora, old_pad = h->r_pad;
+  h->r_lora = r_lora;
+  h->r_pad = rank_pad(rk);
+  const size_t need = h->ws ? ws_layout(h, h->ws_M, h->ws_staging).total : 0;
+  h->r_lora = old_rl;
+  h->r_pad = old_pad;
+  if (h->ws && !h->ws_owned && h->ws_bytes < need)
+    return fail(SVDQ_ERR_WORKSPACE, "the lent workspace is too small for the rank with LoRA (svdq_workspace_size)");
+  std::vector<uint16_t> oldA, oldB;
+  oldA.swap(h->lora_A);
+  oldB.swap(h->lora_B);
+  h->lora_A.swap(A);
+  h->lora_B.swap(B);
+  h->r_lora = r_lora;
+  svdq_status_t st = upload_low_rank(h, static_cast<cudaStream_t>(stream));
+  if (st != SVDQ_OK) {                                      // the device buffers are unchanged
+    h->lora_A.swap(oldA);
+    h->lora_B.swap(oldB);
+    h->r_lora = old_rl;
+    return st;
+  }
+  if (h->ws && h->ws_owned && h->ws_bytes < need) return svdq_reserve(h, h->ws_M, h->ws_staging ? 1 : 0);
+  return SVDQ_OK;
+}
+
 svdq_status_t svdq_reserve(svdq_handle_t h, int64_t M_max, int32_t host_staging) {
   if (!h || M_max < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M_max");
   DeviceGuard guard(h->device);
@@ -466,7 +552,7 @@ svdq_status_t svdq_quantize_act(svdq_handle_t h, const void* X, int64_t M, void*
                                 void* stream) {
   if (!h || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M");
   if (M == 0) return SVDQ_OK;
-  if (!X || !x_codes || !x_scales || (h->host.rank > 0 && !T)) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!X || !x_codes || !x_scales || (h->rank_k() > 0 && !T)) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
   if (!aligned16(X) || !aligned16(x_codes) || !aligned16(x_scales) || (T && !aligned16(T)))
     return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
   if (!h->ws || h->ws_M < M) return fail(SVDQ_ERR_WORKSPACE, "no workspace for this M (svdq_reserve)");
@@ -478,7 +564,7 @@ svdq_status_t svdq_gemm_quantized(svdq_handle_t h, const void* x_codes, const vo
                                   int64_t M, void* stream) {
   if (!h || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M");
   if (M == 0) return SVDQ_OK;
-  if (!x_codes || !x_scales || !Y || (h->host.rank > 0 && !T)) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!x_codes || !x_scales || !Y || (h->rank_k() > 0 && !T)) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
   if (!aligned16(x_codes) || !aligned16(x_scales) || !aligned16(Y) || (T && !aligned16(T)))
     return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
   DeviceGuard guard(h->device);
@@ -497,7 +583,7 @@ svdq_status_t svdq_linear_forward(svdq_handle_t h, const void* X, void* Y, int64
   const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
   void* codes = h->ws + w.codes;
   void* scales = h->ws + w.scales;
-  void* T = h->host.rank ? h->ws + w.T : nullptr;
+  void* T = h->rank_k() ? h->ws + w.T : nullptr;
   svdq_status_t st = launch_k1(h, X, M, codes, scales, T, s);
   if (st != SVDQ_OK) return st;
   return launch_k2(h, codes, scales, T, Y, M, s);
@@ -598,10 +684,10 @@ extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void
   a.LI = h->d_LI;
   a.x_codes = ws + w.codes;
   a.x_scales = ws + w.scales;
-  a.T = h->host.rank ? reinterpret_cast<uint16_t*>(ws + w.T) : nullptr;
+  a.T = h->rank_k() ? reinterpret_cast<uint16_t*>(ws + w.T) : nullptr;
   a.M = M;
   a.K = h->host.K;
-  a.rank = int(h->host.rank);
+  a.rank = int(h->rank_k());
   a.r_pad = int(h->r_pad);
   a.s_gX = h->host.s_gX;
   a.inv_six = h->inv_six;

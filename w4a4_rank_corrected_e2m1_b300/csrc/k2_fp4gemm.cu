@@ -294,10 +294,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int ksteps = krem < 4 ? int(krem) : 4;
             const uint32_t sfa_t = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
             const uint32_t sfb_t = sfa_t + 16;
-            for (int kk = 0; kk < ksteps; ++kk) {
-              ptx::mma2_nvfp4(tmem, ptx::desc_sw128(a_s + 32 * kk), ptx::desc_sw128(b_s + 32 * kk), IDESC_NVFP4,
-                              sfa_t + 4 * kk, sfb_t + 8 * kk, accumulate);
+            if (ksteps == 4) {
+              // full 256-wide K step: descriptors built once, the k-slices 32 bytes apart
+              // (start-address field in 16-byte units)
+              const uint64_t ad = ptx::desc_sw128(a_s), bd = ptx::desc_sw128(b_s);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                ptx::mma2_nvfp4(tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), IDESC_NVFP4, sfa_t + 4 * kk,
+                                sfb_t + 8 * kk, kk == 0 ? accumulate : 1u);
               accumulate = 1;
+            } else {
+              for (int kk = 0; kk < ksteps; ++kk) {
+                ptx::mma2_nvfp4(tmem, ptx::desc_sw128(a_s + 32 * kk), ptx::desc_sw128(b_s + 32 * kk), IDESC_NVFP4,
+                                sfa_t + 4 * kk, sfb_t + 8 * kk, accumulate);
+                accumulate = 1;
+              }
             }
           }
           ptx::tc_commit2_mc(&s->empty[stage], kPairMask);

@@ -46,7 +46,7 @@ class PackedHost(ctypes.Structure):
 
 class Info(ctypes.Structure):
     _fields_ = [
-        ("N", _i64), ("K", _i64), ("rank", _i64), ("r_pad", _i64), ("M_max", _i64),
+        ("N", _i64), ("K", _i64), ("rank", _i64), ("lora_rank", _i64), ("r_pad", _i64), ("M_max", _i64),
         ("s_gW", ctypes.c_float), ("s_gX", ctypes.c_float), ("alpha", ctypes.c_float),
         ("device", _i32), ("sm_count", _i32),
     ]
@@ -67,6 +67,7 @@ _SIGS = {
     "svdq_linear_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_linear_forward_host": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_check_error": (_i32, [_vp]),
+    "svdq_attach_lora": (_i32, [_vp, _vp, _vp, _i64, ctypes.c_float, _vp]),
     "svdq_status_string": (ctypes.c_char_p, [_i32]),
     "svdq_last_error": (ctypes.c_char_p, []),
 }
@@ -246,3 +247,16 @@ class Layer:
 
     def check_error(self):
         check(LIB.svdq_check_error(self.h), "svdq_check_error")
+
+    def attach_lora(self, A, B, scale: float = 1.0, stream=None):
+        """Append a LoRA adapter (A: K x r_lora, B: r_lora x N, bf16 bit patterns on the host)
+        to the low-rank branch; A = B = None removes it."""
+        if A is None:
+            check(LIB.svdq_attach_lora(self.h, None, None, 0, 1.0, _stream(stream)), "svdq_attach_lora")
+            return
+        A, B = _u16(A), _u16(B)
+        r_lora = int(A.shape[1])
+        if A.shape != (self.K, r_lora) or B.shape != (r_lora, self.N):
+            raise ValueError(f"LoRA factors must be {self.K} x r and r x {self.N}")
+        check(LIB.svdq_attach_lora(self.h, A.ctypes.data, B.ctypes.data, r_lora, float(scale), _stream(stream)),
+              "svdq_attach_lora")
