@@ -278,6 +278,39 @@ def test_ragged_n_and_k():
     gh.assert_y_close(Y, sq.forward(d["X"], gh.oracle_packed(exp)), "ragged")
 
 
+def test_tall_path_ragged_m_and_odd_chunk_count():
+    """M large enough for the whole-K 32-row kernel, M % 32 != 0, K with an odd number of
+    64-column chunks (the last stage's second chunk is past K) and K % 256 != 0."""
+    w = synthetic.scaled(synthetic.QKV, name="tall_ragged", M=2413, K=576, N=256, rank=32, n_outlier=6)
+    d, layer, exp = case(w)
+    c, s, t, raw = run_k1(layer, d["X"], w.M)
+    rc, rs, xh = sq.quantize_act(d["X"], exp["inv_lambda"], exp["s_gX"])
+    assert np.array_equal(c, rc) and np.array_equal(s, rs)
+    KG = 4 * -(-w.K // 256)
+    tiles = raw[: -(-w.M // 128) * KG * 512].reshape(-1, KG, 512)
+    assert np.all(tiles[:, w.K // 64:, :] == 0)
+    # T' = (X^ L1) / alpha against the oracle's float64 down-projection
+    tref = sq.lowrank_down(xh, exp["L1"]) / float(exp["alpha"])
+    assert np.max(np.abs(t[:, :w.rank] - tref)) <= 2e-2 * np.max(np.abs(tref))
+    assert np.all(t[:, w.rank:] == 0)
+    Y = run_forward(layer, d["X"], w.M)
+    gh.assert_y_close(Y, sq.forward(d["X"], gh.oracle_packed(exp)), "tall ragged")
+
+
+@pytest.mark.parametrize("w", [synthetic.QKV, synthetic.OPROJ_M[1]], ids=lambda w: w.name)
+def test_k1_bitexact_on_repeated_launches(w):
+    """Kernel 1 run back to back (whole-K 32-row kernel for QKV, split-K kernel for the
+    1024-token o-proj): every launch is bit-exact.  A missing ordering between the
+    quantiser's reads of a stage and the copies that refill it shows up here as a few
+    blocks read from the wrong step."""
+    d, layer, exp = case(w)
+    rc, rs, _ = sq.quantize_act(d["X"], exp["inv_lambda"], exp["s_gX"])
+    for i in range(6):
+        c, s, _, _ = run_k1(layer, d["X"], w.M)
+        assert np.array_equal(s, rs), f"launch {i}: scale mismatches {np.sum(s != rs)}"
+        assert np.array_equal(c, rc), f"launch {i}: code mismatches {np.sum(c != rc)}"
+
+
 # ------------------------------------------------------------------ full FLUX-shaped sizes
 FULL = [synthetic.QKV, synthetic.MLP_UP, synthetic.MLP_DOWN, *synthetic.OPROJ_M, *synthetic.OPROJ_R]
 

@@ -177,9 +177,10 @@ void free_layer(svdq_layer* h) {
 
 // Device layouts of the low-rank branch for the handle's kernel rank (SVD rank plus any LoRA
 // rank), uploaded into fresh buffers that replace the old ones:
-//   LI   per 64-column chunk c: the chunk's slice of L1' (rank_k rows of 64 K-values, bf16,
-//        K-major, 128-byte rows with the 128-byte swizzle the tensor cores read: 16-byte unit u
-//        of row j stored at unit u ^ (j % 8)), then the chunk's 64 values of 1/lambda (fp32).
+//   LI   per pair of 64-column chunks: both chunks' slices of L1' (rank_k rows of 64 K-values,
+//        bf16, K-major, 128-byte rows with the 128-byte swizzle the tensor cores read: 16-byte
+//        unit u of row j stored at unit u ^ (j % 8)), then both chunks' 64 values of 1/lambda
+//        (fp32).
 //        L1' = diag(1/lambda) L1 for the SVD columns (kernel 1 multiplies raw X by it, which
 //        is X^ L1), and bf16(scale * A) for the LoRA columns (X A needs no smoothing)
 //   L2t  N x r_pad bf16: L2 transposed, then B transposed, zero padding
@@ -192,19 +193,23 @@ svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
     for (int64_t j = 0; j < r; ++j) l2t[n * r_pad + j] = hp.L2[j * N + n];
     for (int64_t j = 0; j < rl; ++j) l2t[n * r_pad + r + j] = h->lora_B[j * N + n];
   }
-  const int64_t li_chunk = rk * 128 + 256;
-  std::vector<unsigned char> li(size_t(K / 64) * li_chunk, 0);
-  for (int64_t c = 0; c < K / 64; ++c) {
-    unsigned char* base = li.data() + c * li_chunk;
+  // groups of two chunks (2g, 2g + 1): [slice 2g][slice 2g + 1][1/lambda 2g][1/lambda 2g + 1];
+  // a chunk past K (odd chunk count) stays zero
+  const int64_t nch = K / 64, ngroups = (nch + 1) / 2;
+  const int64_t li_group = 2 * rk * 128 + 512;
+  std::vector<unsigned char> li(size_t(ngroups) * li_group, 0);
+  for (int64_t c = 0; c < nch; ++c) {
+    unsigned char* grp = li.data() + (c / 2) * li_group;
+    unsigned char* slice = grp + (c % 2) * rk * 128;
     for (int64_t j = 0; j < rk; ++j)
       for (int i = 0; i < 64; ++i) {
         const int64_t k = 64 * c + i;
         const uint16_t v = j < r ? f64_to_bf16(double(hp.inv_lambda[k]) * double(bf16_to_f32(hp.L1[k * r + j])))
                                  : h->lora_A[k * rl + (j - r)];
         const int unit = (i / 8) ^ int(j % 8);
-        reinterpret_cast<uint16_t*>(base + j * 128 + unit * 16)[i % 8] = v;
+        reinterpret_cast<uint16_t*>(slice + j * 128 + unit * 16)[i % 8] = v;
       }
-    std::memcpy(base + rk * 128, hp.inv_lambda.data() + 64 * c, 256);
+    std::memcpy(grp + 2 * rk * 128 + (c % 2) * 256, hp.inv_lambda.data() + 64 * c, 256);
   }
   cudaError_t e;
   uint16_t* d_l2t = static_cast<uint16_t*>(dalloc(l2t.size() * 2, &e));

@@ -74,6 +74,56 @@ struct Cfg {
   static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(R >> 3) << 17) | (uint32_t(128 >> 4) << 24);
 };
 
+// The L1 / 1/lambda buffer comes in groups of two 64-column chunks (2c, 2c + 1):
+//   [L1' slice 2c][L1' slice 2c + 1][1/lambda of 2c][1/lambda of 2c + 1]
+// each slice R rows x 128 bytes (bf16, K-major, 128-byte swizzle), each 1/lambda part 64 fp32.
+__host__ __device__ constexpr int64_t li_group_bytes(int R) { return int64_t(2) * R * 128 + 512; }
+
+// Split kernel: chunk c's slice and 1/lambda values into the stage, after its X tile.
+template <int R>
+__device__ __forceinline__ void li_loads(unsigned char* st, const unsigned char* LI, int c, uint64_t* bar) {
+  const unsigned char* g = LI + int64_t(c >> 1) * li_group_bytes(R);
+  constexpr int X_BYTES = 128 * 128, L_BYTES = R * 128;
+  if (R > 0) ptx::bulk_load(st + X_BYTES, g + (c & 1) * L_BYTES, L_BYTES, bar);
+  ptx::bulk_load(st + X_BYTES + L_BYTES, g + 2 * L_BYTES + (c & 1) * 256, 256, bar);
+}
+
+// One 16-element NVFP4 block of a row: w holds its 16 bf16 values (8 words, low half first),
+// il their 1/lambda.  x^ = fl32(x * inv_lambda); scale code s8 = E4M3(fl32(amax / fl32(6 s_gX)))
+// from one product with the reciprocal, settled by the thresholds; codes = E2M1(fl32(x^ * rcp)).
+// Returns s8 and the 16 codes as two words (element 2j in the low nibble of byte j).
+__device__ __forceinline__ uint32_t quant_block(const uint32_t* w, const float* il, float inv_six, const float* s_thr,
+                                                const float* s_rcp, uint32_t* code0, uint32_t* code1) {
+  float2 xh[8];
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float2 xv = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+    xh[k] = ptx::mul2_rn(xv, make_float2(il[2 * k], il[2 * k + 1]));
+    m = fmaxf(m, fmaxf(fabsf(xh[k].x), fabsf(xh[k].y)));
+  }
+  int code = int(ptx::cvt_e4m3x2(0.f, __fmul_rn(m, inv_six)) & 0xFF);
+  code = code - (m < s_thr[code] ? 1 : 0) + (m >= s_thr[code + 1] ? 1 : 0);
+  *code0 = 0u;
+  *code1 = 0u;
+  if (code != 0) {
+    const float rcp = s_rcp[code];
+    const float2 r2 = make_float2(rcp, rcp);
+    float2 q[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) q[k] = ptx::mul2_rn(xh[k], r2);
+    *code0 = ptx::cvt_e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y);
+    *code1 = ptx::cvt_e2m1x8(q[4].x, q[4].y, q[5].x, q[5].y, q[6].x, q[6].y, q[7].x, q[7].y);
+  }
+  return uint32_t(code);
+}
+
+// Byte offset of the 32-bit word holding row `row`'s four scales of 64-column chunk c in the
+// tiled activation-scale layout.
+__device__ __forceinline__ int64_t scale_word_offset(int64_t row, int64_t c, int64_t KG) {
+  return ((row >> 7) * KG + c) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
+}
+
 __device__ bool k1_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -145,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int c = c0; c < nchunks && pre < C::STAGES; c += nsplit, ++pre) {
         unsigned char* st = ring + pre * C::STAGE_BYTES;
         ptx::mbar_arrive_expect_tx(&full[pre], C::X_BYTES + C::LI_BYTES);
-        ptx::bulk_load(st + C::X_BYTES, a.LI + int64_t(c) * C::LI_BYTES, C::LI_BYTES, &full[pre]);
+        li_loads<R>(st, a.LI, c, &full[pre]);
       }
       ptx::griddep_wait();
       int stage = 0, issued = 0;
@@ -154,8 +204,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         unsigned char* st = ring + stage * C::STAGE_BYTES;
         if (issued >= pre) {
           if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err)) break;
+          // the quantiser warps read this stage with ordinary loads before releasing it; the
+          // proxy fence orders those reads before the tensor copies that overwrite it
+          ptx::fence_proxy_async_smem();
           ptx::mbar_arrive_expect_tx(&full[stage], C::X_BYTES + C::LI_BYTES);
-          ptx::bulk_load(st + C::X_BYTES, a.LI + int64_t(c) * C::LI_BYTES, C::LI_BYTES, &full[stage]);
+          li_loads<R>(st, a.LI, c, &full[stage]);
         }
         ptx::tma_load_2d(st, &xmap, &full[stage], 64 * c, int(row0));
         if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -226,28 +279,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int64_t col = int64_t(c) * 64 + 16 * t;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float2 xh[8];
-        float m = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 xv = make_float2(__uint_as_float(w[h][k] << 16), __uint_as_float(w[h][k] & 0xFFFF0000u));
-          xh[k] = ptx::mul2_rn(xv, make_float2(il[2 * k], il[2 * k + 1]));
-          m = fmaxf(m, fmaxf(fabsf(xh[k].x), fabsf(xh[k].y)));
-        }
-        int code = int(ptx::cvt_e4m3x2(0.f, __fmul_rn(m, a.inv_six)) & 0xFF);
-        code = code - (m < s_thr[code] ? 1 : 0) + (m >= s_thr[code + 1] ? 1 : 0);
-        const uint32_t s8 = uint32_t(code);
+        uint32_t code0, code1;
+        const uint32_t s8 = quant_block(w[h], il, a.inv_six, s_thr, s_rcp, &code0, &code1);
         const int64_t row = row0 + 16 * warp + g + 8 * h;
-        uint32_t code0 = 0u, code1 = 0u;
-        if (s8 != 0u) {
-          const float rcp = s_rcp[code];
-          const float2 r2 = make_float2(rcp, rcp);
-          float2 q[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) q[k] = ptx::mul2_rn(xh[k], r2);
-          code0 = ptx::cvt_e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y);
-          code1 = ptx::cvt_e2m1x8(q[4].x, q[4].y, q[5].x, q[5].y, q[6].x, q[6].y, q[7].x, q[7].y);
-        }
         if (row < M) {
           uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + col / 2);
           *dst = make_uint2(code0, code1);
@@ -256,20 +290,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t word = s8 << (8 * t);
         word |= __shfl_xor_sync(kFull, word, 1);
         word |= __shfl_xor_sync(kFull, word, 2);
-        if (t == h) {
-          const int64_t off = ((row >> 7) * KG + c) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
-          *reinterpret_cast<uint32_t*>(a.x_scales + off) = word;
-        }
+        if (t == h) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word;
       }
     }
     // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM
     if (split == nsplit - 1) {
       for (int c = nchunks; c < KG; ++c) {
         const int64_t row = row0 + 16 * warp + g + 8 * t;
-        if (t < 2) {
-          const int64_t off = ((row >> 7) * KG + c) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
-          *reinterpret_cast<uint32_t*>(a.x_scales + off) = 0u;
-        }
+        if (t < 2) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = 0u;
       }
     }
   }
@@ -362,6 +390,243 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// ------------------------------------------------------------------ tall kernel
+// For M large enough to fill the GPU with 32-row tiles, a CTA takes 32 rows and the whole of
+// K, so the down-projection needs no split and no cross-CTA reduction.  A stage is two
+// 64-column chunks: two 32 x 64 X tiles (TMA) and one LI group (bulk copy).  The
+// down-projection uses tcgen05.mma with M = 128: rows 32..127 of the A operand run into the
+// following shared memory and only produce TMEM lanes 32..127, which nothing reads (the ring
+// is followed by a pad so those reads stay inside the CTA's shared memory).
+constexpr int kTallRows = 32;
+
+template <int R>
+struct TallCfg {
+  static constexpr int X_TILE = kTallRows * 128;               // 32 rows x 64 bf16
+  static constexpr int X_BYTES = 2 * X_TILE;
+  static constexpr int L_BYTES = R * 128;
+  static constexpr int LI_BYTES = int(li_group_bytes(R));
+  static constexpr int STAGE_BYTES = ((X_BYTES + LI_BYTES + 1023) / 1024) * 1024;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+  static constexpr int SPAN = X_TILE + 128 * 128;               // farthest A byte read: tile 1 + 128 rows
+  static constexpr int PAD = SPAN > STAGE_BYTES ? SPAN - STAGE_BYTES : 0;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + PAD + 1024;
+  static constexpr uint32_t TMEM_COLS = R <= 32 ? 32 : (R <= 64 ? 64 : 128);
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(R >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+};
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1)
+    k1_tall_kernel(const __grid_constant__ XMap xmap, K1Args a) {
+  using C = TallCfg<R>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], done;
+  __shared__ volatile int abort_flag;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float s_thr[128], s_rcp[128];
+
+  ptx::griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t M = a.M, K = a.K;
+  const int64_t KG = scale_groups(K);
+  const int nchunks = int(K / 64);
+  const int nsteps = (nchunks + 1) / 2;
+  const int64_t row0 = int64_t(blockIdx.x) * kTallRows;
+
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) (i < 128 ? s_thr[i] : s_rcp[i - 128]) = a.qtab[i];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], kQWarps + (R > 0 ? 1 : 0));
+    }
+    ptx::mbar_init(&done, 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (R > 0 && warp == kMma) {
+    ptx::tmem_alloc(&tmem_slot, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp != kProducer) ptx::griddep_wait();
+
+  if (warp == kProducer) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&xmap);
+      // the LI groups of the first ring pass are constants: requested before the grid wait
+      const int pre = nsteps < C::STAGES ? nsteps : C::STAGES;
+      for (int st_i = 0; st_i < pre; ++st_i) {
+        unsigned char* st = ring + st_i * C::STAGE_BYTES;
+        ptx::mbar_arrive_expect_tx(&full[st_i], C::X_BYTES + C::LI_BYTES);
+        ptx::bulk_load(st + C::X_BYTES, a.LI + int64_t(st_i) * C::LI_BYTES, C::LI_BYTES, &full[st_i]);
+      }
+      ptx::griddep_wait();
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int j = 0; j < nsteps; ++j, ++issued) {
+        unsigned char* st = ring + stage * C::STAGE_BYTES;
+        if (j >= pre) {
+          if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err)) break;
+          ptx::fence_proxy_async_smem();   // ordinary-load reads of the stage before the refill
+          ptx::mbar_arrive_expect_tx(&full[stage], C::X_BYTES + C::LI_BYTES);
+          ptx::bulk_load(st + C::X_BYTES, a.LI + int64_t(j) * C::LI_BYTES, C::LI_BYTES, &full[stage]);
+        }
+        // a chunk index past K reads as zeros (out-of-range box) and still delivers its bytes
+        ptx::tma_load_2d(st, &xmap, &full[stage], 128 * j, int(row0));
+        ptx::tma_load_2d(st + C::X_TILE, &xmap, &full[stage], 128 * j + 64, int(row0));
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      for (int i = 0; i < C::STAGES; ++i) {       // every copy issued has landed
+        const int used = issued - i;
+        if (used <= 0) continue;
+        const uint32_t last_parity = uint32_t(((used - 1) / C::STAGES) & 1);
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(&full[i], last_parity))
+          if (ptx::globaltimer() - t0 > kTimeoutNs) break;
+      }
+    }
+  } else if (warp == kMma) {
+    // ------------------------------------------------------------ MMA issuer (down-projection)
+    if (R > 0 && lane == 0) {
+      const uint32_t tmem = tmem_slot;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t accumulate = 0;
+      for (int j = 0; j < nsteps; ++j) {
+        if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
+        ptx::tc_fence_after();
+        const uint32_t xs = ptx::smem_u32(ring + stage * C::STAGE_BYTES);
+        const uint32_t ls = xs + C::X_BYTES;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            ptx::mma_bf16(tmem, ptx::desc_sw128(xs + cc * C::X_TILE + 32 * kk),
+                          ptx::desc_sw128(ls + cc * C::L_BYTES + 32 * kk), C::IDESC, accumulate);
+            accumulate = 1;
+          }
+        ptx::tc_commit(&empty[stage]);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      ptx::tc_commit(&done);
+    }
+  } else {
+    // ------------------------------------------------------------ quantiser warps
+    // warp w takes chunk w / 4 of the stage and rows 8 (w % 4) .. + 7; thread (g, t) one
+    // 16-element block: row 8 (w % 4) + g, columns 16 t .. 16 t + 15 of the chunk
+    const int cc = warp >> 2;
+    const int r = 8 * (warp & 3) + g;
+    const int64_t row = row0 + r;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < nsteps; ++j) {
+      if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
+      const unsigned char* st = ring + stage * C::STAGE_BYTES;
+      uint32_t w[8];
+      float il[16];
+      {
+        const unsigned char* rowp = st + cc * C::X_TILE + r * 128;
+        const uint4 u0 = *reinterpret_cast<const uint4*>(rowp + (((2 * t) ^ (r & 7)) << 4));
+        const uint4 u1 = *reinterpret_cast<const uint4*>(rowp + (((2 * t + 1) ^ (r & 7)) << 4));
+        w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
+        w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+        const float4* p = reinterpret_cast<const float4*>(st + C::X_BYTES + 2 * C::L_BYTES + cc * 256) + 4 * t;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 v = p[k];
+          il[4 * k] = v.x; il[4 * k + 1] = v.y; il[4 * k + 2] = v.z; il[4 * k + 3] = v.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[stage]);
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+
+      const int c = 2 * j + cc;
+      if (c >= nchunks) continue;
+      uint32_t code0, code1;
+      const uint32_t s8 = quant_block(w, il, a.inv_six, s_thr, s_rcp, &code0, &code1);
+      if (row < M) {
+        uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + (int64_t(c) * 64 + 16 * t) / 2);
+        *dst = make_uint2(code0, code1);
+      }
+      uint32_t word = s8 << (8 * t);
+      word |= __shfl_xor_sync(kFull, word, 1);
+      word |= __shfl_xor_sync(kFull, word, 2);
+      if (t == 0) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word;
+    }
+    // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM
+    for (int c = nchunks; c < KG; ++c)
+      if ((c & 1) == cc && t == 0) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = 0u;
+  }
+
+  // ---- T = (X^ L1) / alpha for the CTA's 32 rows, straight from TMEM lanes 0..31
+  if constexpr (R > 0) {
+    if (warp == 0) {
+      const bool ok = k1_wait(&done, 0, &abort_flag, a.err);
+      ptx::tc_fence_after();
+      const int64_t row = row0 + lane;
+      const int r_pad = a.r_pad;
+#pragma unroll
+      for (int cb = 0; cb < R; cb += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tmem_slot + cb, v);
+        ptx::tmem_wait_ld();
+        if (row < M) {
+          uint4* dst = reinterpret_cast<uint4*>(a.T + row * r_pad + cb);
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            if (cb + j < R) {
+              uint32_t o[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                o[u] = ok ? ptx::pack_bf16x2(__uint_as_float(v[j + 2 * u]) * a.inv_alpha,
+                                             __uint_as_float(v[j + 2 * u + 1]) * a.inv_alpha)
+                          : 0u;
+              dst[j / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        }
+      }
+      if (row < M)
+        for (int j = R; j < r_pad; j += 8) reinterpret_cast<uint4*>(a.T + row * r_pad + j)[0] = make_uint4(0, 0, 0, 0);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMma) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc(tmem_slot, C::TMEM_COLS);
+    }
+  }
+}
+
+template <int R>
+int launch_tall(const XMap& map, const K1Args& a, const K1Plan& p, cudaStream_t s) {
+  using C = TallCfg<R>;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k1_tall_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return int(e);
+    attr_done[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.row_tiles, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return int(cudaLaunchKernelEx(&cfg, k1_tall_kernel<R>, map, a));
+}
+
 template <int R>
 int launch_t(const XMap& map, const K1Args& a, const K1Plan& p, cudaStream_t s) {
   using C = Cfg<R>;
@@ -393,9 +658,17 @@ int launch_t(const XMap& map, const K1Args& a, const K1Plan& p, cudaStream_t s) 
 K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count) {
   (void)rank;
   K1Plan p;
-  p.row_tiles = int(ceil_div(M, kRows));
   const int nchunks = int(K / 64);
-  // K splits per row tile: fill one wave of resident CTAs (two per SM), at most kK1MaxSplit,
+  // enough 32-row tiles to give every other SM one: whole-K CTAs, no split
+  if (ceil_div(M, kTallRows) * 2 >= sm_count) {
+    p.tall = true;
+    p.row_tiles = int(ceil_div(M, kTallRows));
+    p.nsplit = 1;
+    p.chunks_per_split = nchunks;
+    return p;
+  }
+  p.row_tiles = int(ceil_div(M, kRows));
+  // K splits per 128-row tile: fill one wave of resident CTAs (two per SM), at most kK1MaxSplit,
   // at most the chunk count
   const int slots = 2 * sm_count;
   int ns = p.row_tiles > 0 ? slots / p.row_tiles : 1;
@@ -414,20 +687,24 @@ size_t k1_arrival_bytes(int64_t M) { return size_t(ceil_div(M, kRows)) * sizeof(
 int k1_launch(const K1Args& a, const K1Plan& p, void* stream, std::string* err) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   XMap map;
-  if (!encode_map_2d(map.m, 2, a.X, uint64_t(a.K), uint64_t(a.M), uint64_t(a.K) * 2, 64, uint32_t(kRows), 1, err))
+  const uint32_t box_rows = p.tall ? uint32_t(kTallRows) : uint32_t(kRows);
+  if (!encode_map_2d(map.m, 2, a.X, uint64_t(a.K), uint64_t(a.M), uint64_t(a.K) * 2, 64, box_rows, 1, err))
     return -1;
+#define SVDQ_K1_CASE(R) \
+  case R: return p.tall ? launch_tall<R>(map, a, p, s) : launch_t<R>(map, a, p, s);
   switch (a.rank) {
-    case 0: return launch_t<0>(map, a, p, s);
-    case 16: return launch_t<16>(map, a, p, s);
-    case 32: return launch_t<32>(map, a, p, s);
-    case 48: return launch_t<48>(map, a, p, s);
-    case 64: return launch_t<64>(map, a, p, s);
-    case 80: return launch_t<80>(map, a, p, s);
-    case 96: return launch_t<96>(map, a, p, s);
-    case 112: return launch_t<112>(map, a, p, s);
-    case 128: return launch_t<128>(map, a, p, s);
+    SVDQ_K1_CASE(0)
+    SVDQ_K1_CASE(16)
+    SVDQ_K1_CASE(32)
+    SVDQ_K1_CASE(48)
+    SVDQ_K1_CASE(64)
+    SVDQ_K1_CASE(80)
+    SVDQ_K1_CASE(96)
+    SVDQ_K1_CASE(112)
+    SVDQ_K1_CASE(128)
     default: return int(cudaErrorInvalidValue);
   }
+#undef SVDQ_K1_CASE
 }
 
 }  // namespace svdq

@@ -55,7 +55,7 @@ SVDQ_HD inline int64_t rank_pad(int64_t r) { return r == 0 ? 0 : round_up(r, 64)
 // ------------------------------------------------------------------ kernel 1 (k1_actquant.cu)
 struct K1Args {
   const uint16_t* X;          // M x K bf16 (read through the tensor map passed beside these args)
-  const unsigned char* LI;    // per 64-column chunk: swizzled L1' slice (rank x 128 B) then 1/lambda (256 B)
+  const unsigned char* LI;    // per pair of 64-column chunks: two swizzled L1' slices (rank x 128 B), two 1/lambda parts
   uint8_t* x_codes;           // M x K/2
   uint8_t* x_scales;          // tiled
   uint16_t* T;                // M x r_pad bf16 (null if rank == 0)
@@ -69,6 +69,7 @@ struct K1Args {
   int* err;                   // device error word (bounded waits)
 };
 struct K1Plan {
+  bool tall = false;          // 32-row tiles over the whole of K (no split) instead of 128-row split tiles
   int row_tiles = 0, nsplit = 1, chunks_per_split = 1;
 };
 K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count);
