@@ -177,10 +177,10 @@ void free_layer(svdq_layer* h) {
 
 // Device layouts of the low-rank branch for the handle's kernel rank (SVD rank plus any LoRA
 // rank), uploaded into fresh buffers that replace the old ones:
-//   LI   per pair of 64-column chunks: both chunks' slices of L1' (rank_k rows of 64 K-values,
-//        bf16, K-major, 128-byte rows with the 128-byte swizzle the tensor cores read: 16-byte
-//        unit u of row j stored at unit u ^ (j % 8)), then both chunks' 64 values of 1/lambda
-//        (fp32).
+//   LI   per group of four 64-column chunks: the chunks' slices of L1' (rank_k rows of 64
+//        K-values, bf16, K-major, 128-byte rows with the 128-byte swizzle the tensor cores
+//        read: 16-byte unit u of row j stored at unit u ^ (j % 8)), then the chunks' 64 values
+//        of 1/lambda each (fp32).
 //        L1' = diag(1/lambda) L1 for the SVD columns (kernel 1 multiplies raw X by it, which
 //        is X^ L1), and bf16(scale * A) for the LoRA columns (X A needs no smoothing)
 //   L2t  N x r_pad bf16: L2 transposed, then B transposed, zero padding
@@ -193,14 +193,14 @@ svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
     for (int64_t j = 0; j < r; ++j) l2t[n * r_pad + j] = hp.L2[j * N + n];
     for (int64_t j = 0; j < rl; ++j) l2t[n * r_pad + r + j] = h->lora_B[j * N + n];
   }
-  // groups of two chunks (2g, 2g + 1): [slice 2g][slice 2g + 1][1/lambda 2g][1/lambda 2g + 1];
-  // a chunk past K (odd chunk count) stays zero
-  const int64_t nch = K / 64, ngroups = (nch + 1) / 2;
-  const int64_t li_group = 2 * rk * 128 + 512;
+  // groups of four chunks (4g .. 4g + 3): [the four slices][the four 1/lambda parts]; a chunk
+  // past K stays zero
+  const int64_t nch = K / 64, ngroups = (nch + 3) / 4;
+  const int64_t li_group = 4 * (rk * 128 + 256);
   std::vector<unsigned char> li(size_t(ngroups) * li_group, 0);
   for (int64_t c = 0; c < nch; ++c) {
-    unsigned char* grp = li.data() + (c / 2) * li_group;
-    unsigned char* slice = grp + (c % 2) * rk * 128;
+    unsigned char* grp = li.data() + (c / 4) * li_group;
+    unsigned char* slice = grp + (c % 4) * rk * 128;
     for (int64_t j = 0; j < rk; ++j)
       for (int i = 0; i < 64; ++i) {
         const int64_t k = 64 * c + i;
@@ -209,7 +209,7 @@ svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
         const int unit = (i / 8) ^ int(j % 8);
         reinterpret_cast<uint16_t*>(slice + j * 128 + unit * 16)[i % 8] = v;
       }
-    std::memcpy(grp + 2 * rk * 128 + (c % 2) * 256, hp.inv_lambda.data() + 64 * c, 256);
+    std::memcpy(grp + 4 * rk * 128 + (c % 4) * 256, hp.inv_lambda.data() + 64 * c, 256);
   }
   cudaError_t e;
   uint16_t* d_l2t = static_cast<uint16_t*>(dalloc(l2t.size() * 2, &e));

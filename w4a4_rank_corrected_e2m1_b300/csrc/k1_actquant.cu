@@ -74,18 +74,20 @@ struct Cfg {
   static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(R >> 3) << 17) | (uint32_t(128 >> 4) << 24);
 };
 
-// The L1 / 1/lambda buffer comes in groups of two 64-column chunks (2c, 2c + 1):
-//   [L1' slice 2c][L1' slice 2c + 1][1/lambda of 2c][1/lambda of 2c + 1]
+// The L1 / 1/lambda buffer comes in groups of four 64-column chunks (4g .. 4g + 3):
+//   [L1' slices of the four chunks][1/lambda of the four chunks]
 // each slice R rows x 128 bytes (bf16, K-major, 128-byte swizzle), each 1/lambda part 64 fp32.
-__host__ __device__ constexpr int64_t li_group_bytes(int R) { return int64_t(2) * R * 128 + 512; }
+constexpr int kLIGroup = 4;
+__host__ __device__ constexpr int64_t li_group_bytes(int R) { return int64_t(kLIGroup) * (R * 128 + 256); }
 
 // Split kernel: chunk c's slice and 1/lambda values into the stage, after its X tile.
 template <int R>
 __device__ __forceinline__ void li_loads(unsigned char* st, const unsigned char* LI, int c, uint64_t* bar) {
-  const unsigned char* g = LI + int64_t(c >> 1) * li_group_bytes(R);
+  const unsigned char* g = LI + int64_t(c / kLIGroup) * li_group_bytes(R);
+  const int i = c % kLIGroup;
   constexpr int X_BYTES = 128 * 128, L_BYTES = R * 128;
-  if (R > 0) ptx::bulk_load(st + X_BYTES, g + (c & 1) * L_BYTES, L_BYTES, bar);
-  ptx::bulk_load(st + X_BYTES + L_BYTES, g + 2 * L_BYTES + (c & 1) * 256, 256, bar);
+  if (R > 0) ptx::bulk_load(st + X_BYTES, g + i * L_BYTES, L_BYTES, bar);
+  ptx::bulk_load(st + X_BYTES + L_BYTES, g + kLIGroup * L_BYTES + i * 256, 256, bar);
 }
 
 // One 16-element NVFP4 block of a row: w holds its 16 bf16 values (8 words, low half first),
@@ -392,27 +394,48 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // ------------------------------------------------------------------ tall kernel
 // For M large enough to fill the GPU with 32-row tiles, a CTA takes 32 rows and the whole of
-// K, so the down-projection needs no split and no cross-CTA reduction.  A stage is two
-// 64-column chunks: two 32 x 64 X tiles (TMA) and one LI group (bulk copy).  The
-// down-projection uses tcgen05.mma with M = 128: rows 32..127 of the A operand run into the
-// following shared memory and only produce TMEM lanes 32..127, which nothing reads (the ring
-// is followed by a pad so those reads stay inside the CTA's shared memory).
+// K, so the down-projection needs no split and no cross-CTA reduction.  A stage is CH
+// consecutive 64-column chunks (CH x 128 contiguous bytes of every row, so DRAM pages are
+// read in long runs): CH 32 x 64 X tiles (TMA) and the chunks' L1 slices and 1/lambda parts
+// (bulk copies).  The down-projection uses tcgen05.mma with M = 128: rows 32..127 of the A
+// operand run into the following shared memory and only produce TMEM lanes 32..127, which
+// nothing reads (the ring is followed by a pad so those reads stay inside the CTA's shared
+// memory).
 constexpr int kTallRows = 32;
 
 template <int R>
 struct TallCfg {
+  static constexpr int CH = R <= 64 ? 4 : 2;                    // chunks per stage
   static constexpr int X_TILE = kTallRows * 128;               // 32 rows x 64 bf16
-  static constexpr int X_BYTES = 2 * X_TILE;
+  static constexpr int X_BYTES = CH * X_TILE;
   static constexpr int L_BYTES = R * 128;
-  static constexpr int LI_BYTES = int(li_group_bytes(R));
+  static constexpr int LI_BYTES = CH * (L_BYTES + 256);
   static constexpr int STAGE_BYTES = ((X_BYTES + LI_BYTES + 1023) / 1024) * 1024;
-  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
-  static constexpr int SPAN = X_TILE + 128 * 128;               // farthest A byte read: tile 1 + 128 rows
+  static constexpr int STAGES = (204 * 1024) / STAGE_BYTES > 8 ? 8 : (204 * 1024) / STAGE_BYTES;
+  static constexpr int SPAN = (CH - 1) * X_TILE + 128 * 128;    // farthest A byte read: last tile + 128 rows
   static constexpr int PAD = SPAN > STAGE_BYTES ? SPAN - STAGE_BYTES : 0;
   static constexpr int SMEM = STAGES * STAGE_BYTES + PAD + 1024;
+  static constexpr int WPC = kQWarps / CH;                     // quantiser warps per chunk
+  static constexpr int RPT = kTallRows / WPC / 8;              // rows per thread
   static constexpr uint32_t TMEM_COLS = R <= 32 ? 32 : (R <= 64 ? 64 : 128);
   static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(R >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+  static_assert(STAGES >= 3, "stages");
 };
+
+// Stage j's L1 slices and 1/lambda parts: [CH slices][CH 1/lambda parts].
+template <int R>
+__device__ __forceinline__ void tall_li_loads(unsigned char* dst, const unsigned char* LI, int j, uint64_t* bar) {
+  using C = TallCfg<R>;
+  const int c0 = C::CH * j;
+  const unsigned char* g = LI + int64_t(c0 / kLIGroup) * li_group_bytes(R);
+  const int i = c0 % kLIGroup;
+  if (C::CH == kLIGroup) {
+    ptx::bulk_load(dst, g, C::LI_BYTES, bar);
+  } else {
+    if (R > 0) ptx::bulk_load(dst, g + i * C::L_BYTES, C::CH * C::L_BYTES, bar);
+    ptx::bulk_load(dst + C::CH * C::L_BYTES, g + kLIGroup * C::L_BYTES + i * 256, C::CH * 256, bar);
+  }
+}
 
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -431,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t M = a.M, K = a.K;
   const int64_t KG = scale_groups(K);
   const int nchunks = int(K / 64);
-  const int nsteps = (nchunks + 1) / 2;
+  const int nsteps = (nchunks + C::CH - 1) / C::CH;
   const int64_t row0 = int64_t(blockIdx.x) * kTallRows;
 
   for (int i = threadIdx.x; i < 256; i += blockDim.x) (i < 128 ? s_thr[i] : s_rcp[i - 128]) = a.qtab[i];
@@ -457,12 +480,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       ptx::prefetch_tmap(&xmap);
-      // the LI groups of the first ring pass are constants: requested before the grid wait
+      // the L1 / 1/lambda parts of the first ring pass are constants: requested before the
+      // grid wait
       const int pre = nsteps < C::STAGES ? nsteps : C::STAGES;
       for (int st_i = 0; st_i < pre; ++st_i) {
         unsigned char* st = ring + st_i * C::STAGE_BYTES;
         ptx::mbar_arrive_expect_tx(&full[st_i], C::X_BYTES + C::LI_BYTES);
-        ptx::bulk_load(st + C::X_BYTES, a.LI + int64_t(st_i) * C::LI_BYTES, C::LI_BYTES, &full[st_i]);
+        tall_li_loads<R>(st + C::X_BYTES, a.LI, st_i, &full[st_i]);
       }
       ptx::griddep_wait();
       int stage = 0, issued = 0;
@@ -473,11 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err)) break;
           ptx::fence_proxy_async_smem();   // ordinary-load reads of the stage before the refill
           ptx::mbar_arrive_expect_tx(&full[stage], C::X_BYTES + C::LI_BYTES);
-          ptx::bulk_load(st + C::X_BYTES, a.LI + int64_t(j) * C::LI_BYTES, C::LI_BYTES, &full[stage]);
+          tall_li_loads<R>(st + C::X_BYTES, a.LI, j, &full[stage]);
         }
         // a chunk index past K reads as zeros (out-of-range box) and still delivers its bytes
-        ptx::tma_load_2d(st, &xmap, &full[stage], 128 * j, int(row0));
-        ptx::tma_load_2d(st + C::X_TILE, &xmap, &full[stage], 128 * j + 64, int(row0));
+#pragma unroll
+        for (int cc = 0; cc < C::CH; ++cc)
+          ptx::tma_load_2d(st + cc * C::X_TILE, &xmap, &full[stage], 64 * (C::CH * j + cc), int(row0));
         if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
       }
       for (int i = 0; i < C::STAGES; ++i) {       // every copy issued has landed
@@ -502,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t xs = ptx::smem_u32(ring + stage * C::STAGE_BYTES);
         const uint32_t ls = xs + C::X_BYTES;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc)
+        for (int cc = 0; cc < C::CH; ++cc)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             ptx::mma_bf16(tmem, ptx::desc_sw128(xs + cc * C::X_TILE + 32 * kk),
@@ -516,25 +541,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ quantiser warps
-    // warp w takes chunk w / 4 of the stage and rows 8 (w % 4) .. + 7; thread (g, t) one
-    // 16-element block: row 8 (w % 4) + g, columns 16 t .. 16 t + 15 of the chunk
-    const int cc = warp >> 2;
-    const int r = 8 * (warp & 3) + g;
-    const int64_t row = row0 + r;
+    // warp w takes chunk w / WPC of the stage and 32 / WPC of its rows; thread (g, t) takes
+    // the 16-element block at columns 16 t .. 16 t + 15 of rows rbase + g + 8 h, h < RPT
+    const int cc = warp / C::WPC;
+    const int rbase = (warp % C::WPC) * (kTallRows / C::WPC);
     int stage = 0;
     uint32_t phase = 0;
     for (int j = 0; j < nsteps; ++j) {
       if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
       const unsigned char* st = ring + stage * C::STAGE_BYTES;
-      uint32_t w[8];
+      uint32_t w[C::RPT][8];
       float il[16];
-      {
+#pragma unroll
+      for (int h = 0; h < C::RPT; ++h) {
+        const int r = rbase + g + 8 * h;
         const unsigned char* rowp = st + cc * C::X_TILE + r * 128;
-        const uint4 u0 = *reinterpret_cast<const uint4*>(rowp + (((2 * t) ^ (r & 7)) << 4));
-        const uint4 u1 = *reinterpret_cast<const uint4*>(rowp + (((2 * t + 1) ^ (r & 7)) << 4));
-        w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
-        w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
-        const float4* p = reinterpret_cast<const float4*>(st + C::X_BYTES + 2 * C::L_BYTES + cc * 256) + 4 * t;
+        const uint4 u0 = *reinterpret_cast<const uint4*>(rowp + (((2 * t) ^ g) << 4));
+        const uint4 u1 = *reinterpret_cast<const uint4*>(rowp + (((2 * t + 1) ^ g) << 4));
+        w[h][0] = u0.x; w[h][1] = u0.y; w[h][2] = u0.z; w[h][3] = u0.w;
+        w[h][4] = u1.x; w[h][5] = u1.y; w[h][6] = u1.z; w[h][7] = u1.w;
+      }
+      {
+        const float4* p = reinterpret_cast<const float4*>(st + C::X_BYTES + C::CH * C::L_BYTES + cc * 256) + 4 * t;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float4 v = p[k];
@@ -545,22 +573,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ptx::mbar_arrive(&empty[stage]);
       if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
 
-      const int c = 2 * j + cc;
+      const int c = C::CH * j + cc;
       if (c >= nchunks) continue;
-      uint32_t code0, code1;
-      const uint32_t s8 = quant_block(w, il, a.inv_six, s_thr, s_rcp, &code0, &code1);
-      if (row < M) {
-        uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + (int64_t(c) * 64 + 16 * t) / 2);
-        *dst = make_uint2(code0, code1);
+#pragma unroll
+      for (int h = 0; h < C::RPT; ++h) {
+        const int64_t row = row0 + rbase + g + 8 * h;
+        uint32_t code0, code1;
+        const uint32_t s8 = quant_block(w[h], il, a.inv_six, s_thr, s_rcp, &code0, &code1);
+        if (row < M) {
+          uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + (int64_t(c) * 64 + 16 * t) / 2);
+          *dst = make_uint2(code0, code1);
+        }
+        uint32_t word = s8 << (8 * t);
+        word |= __shfl_xor_sync(kFull, word, 1);
+        word |= __shfl_xor_sync(kFull, word, 2);
+        if (t == h) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word;
       }
-      uint32_t word = s8 << (8 * t);
-      word |= __shfl_xor_sync(kFull, word, 1);
-      word |= __shfl_xor_sync(kFull, word, 2);
-      if (t == 0) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word;
     }
     // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM
     for (int c = nchunks; c < KG; ++c)
-      if ((c & 1) == cc && t == 0) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = 0u;
+      if (c % C::CH == cc && t < C::RPT)
+        *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row0 + rbase + g + 8 * t, c, KG)) = 0u;
   }
 
   // ---- T = (X^ L1) / alpha for the CTA's 32 rows, straight from TMEM lanes 0..31

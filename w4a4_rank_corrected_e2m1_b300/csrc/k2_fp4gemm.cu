@@ -256,9 +256,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           uint64_t* fb = &s->full[stage];
           if (!(tile == pair && it < pre)) {
             if (!wait_bounded(&s->empty[stage], phase ^ 1u, s, a.err)) { ok = false; break; }
-            // the scale warps read this stage's scales with ordinary loads; the proxy fence
-            // orders those reads before the tensor copies that overwrite the stage
-            ptx::fence_proxy_async_smem();
+            // No proxy fence is needed before overwriting the stage: the scale warps' ordinary
+            // loads of its scales have completed before the stage is released (their values
+            // went into tcgen05.st and tcgen05.wait::st returned before the warps arrived on
+            // "ready", which precedes the MMAs whose commit frees the stage).
             weight_loads(it, n0, nb, st, fb);
           }
           act_loads(it, m0, st, fb);

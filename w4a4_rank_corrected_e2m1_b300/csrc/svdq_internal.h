@@ -55,7 +55,7 @@ SVDQ_HD inline int64_t rank_pad(int64_t r) { return r == 0 ? 0 : round_up(r, 64)
 // ------------------------------------------------------------------ kernel 1 (k1_actquant.cu)
 struct K1Args {
   const uint16_t* X;          // M x K bf16 (read through the tensor map passed beside these args)
-  const unsigned char* LI;    // per pair of 64-column chunks: two swizzled L1' slices (rank x 128 B), two 1/lambda parts
+  const unsigned char* LI;    // per group of four 64-column chunks: four swizzled L1' slices (rank x 128 B), four 1/lambda parts
   uint8_t* x_codes;           // M x K/2
   uint8_t* x_scales;          // tiled
   uint16_t* T;                // M x r_pad bf16 (null if rank == 0)
