@@ -247,6 +247,60 @@ svdq_status_t svdq_check_error(svdq_handle_t h);
 const char* svdq_status_string(svdq_status_t s);
 const char* svdq_last_error(void);
 
+/* ==================================================================================
+ * AWQ-style W4A16 linear layer (the modulation / adaptive-normalisation layers)
+ *
+ * The pages keep 16-bit activations and quantise only the weights to four bits, AWQ style,
+ * for the layers that are more sensitive to precision (aiflownews article on Nunchaku, "How
+ * Nunchaku four bit quantization actually works").  Readings (the pages give none):
+ *   - weights W diag(s) in groups of 64 consecutive input channels of an output row:
+ *     asymmetric 4-bit codes q in [0, 15], float32 scale sc and zero point z in [0, 15]:
+ *       sc = fl32(max(w_max - w_min, 1e-5) / 15), z = clamp(rint(-w_min / sc), 0, 15),
+ *       q = clamp(rint(w / sc) + z, 0, 15)
+ *   - activation-aware per-channel scales s_c = a_c^alpha / sqrt(max s * min s),
+ *     a_c = mean_m |Xcal_mc|, alpha in {0, 0.05, ..., 0.95} picked by the smallest
+ *     calibration output error (all ones without calibration data)
+ *   - forward: x' = fl32(x * fl32(1 / s_c)), Y = x' ((q - z) sc)^T + b, float32 accumulation,
+ *     bf16 out.  Built for the small-M (GEMV-like) modulation shapes: the weights are
+ *     streamed from HBM once per 8 rows of X.
+ * ================================================================================== */
+typedef struct svdq_awq_layer* svdq_awq_handle_t;
+
+typedef struct {
+  int64_t N, K;                /* K % 64 == 0                                                 */
+  const uint16_t* W_bf16;      /* host, N x K row-major                                       */
+  const uint16_t* bias_bf16;   /* host, N, NULL = zero bias                                   */
+  const uint16_t* Xcal_bf16;   /* host, Mcal x K calibration activations, NULL = no search    */
+  int64_t Mcal;
+  const float* s;              /* host, K: per-channel scales to use instead of the search    */
+  int32_t device;
+  void* stream;                /* cudaStream_t for the upload                                 */
+} svdq_awq_params_t;
+
+typedef struct {
+  float* s;                    /* K                                                           */
+  float* inv_s;                /* K, fl32(1 / s)                                              */
+  uint8_t* codes;              /* N x K/2, element 2j in the low nibble of byte j             */
+  float* scales;               /* N x K/64                                                    */
+  uint8_t* zeros;              /* N x K/64                                                    */
+  uint16_t* bias_bf16;         /* N                                                           */
+  float alpha;                 /* searched exponent, -1 if none                               */
+} svdq_awq_host_t;
+
+/* Host quantisation alone (no CUDA call); all outputs in caller buffers.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE. */
+svdq_status_t svdq_awq_pack_host(const svdq_awq_params_t* p, svdq_awq_host_t* out);
+/* svdq_awq_pack_host, then the packed weights uploaded to handle-owned device memory.
+ * Errors: as svdq_awq_pack_host, plus ARCH, OOM, CUDA. */
+svdq_status_t svdq_awq_pack(const svdq_awq_params_t* p, svdq_awq_handle_t* out);
+svdq_status_t svdq_awq_destroy(svdq_awq_handle_t h);
+/* Copy of the packed layer (buffers as in svdq_awq_host_t, caller-owned). */
+svdq_status_t svdq_awq_export(svdq_awq_handle_t h, svdq_awq_host_t* out);
+/* Y (device, M x N bf16) = x' W'^T + b for X (device, M x K bf16); asynchronous on stream,
+ * allocates nothing; X and Y 16-byte aligned, not aliased; M = 0 is a no-op.
+ * Errors: INVALID_ARG, CUDA. */
+svdq_status_t svdq_awq_forward(svdq_awq_handle_t h, const void* X_bf16, void* Y_bf16, int64_t M, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -118,3 +118,56 @@ def test_randomized_svd_near_eckart_young(shape):
     cw, sw = nvfp4.quantize_blocks(R, nvfp4.global_scale(np.max(np.abs(R))))
     assert np.array_equal(got["R_codes"], (cw[:, 0::2] | (cw[:, 1::2] << 4)).astype(np.uint8))
     assert np.array_equal(got["R_scales"], sw)
+
+
+# ------------------------------------------------------------------ AWQ-style W4A16 host pack
+def _awq_case(seed, N=48, K=256, M=24):
+    rng = np.random.default_rng(seed)
+    W = sq.f64_to_bf16(rng.standard_normal((N, K)) * 0.05)
+    W[:, 5] = sq.f64_to_bf16(np.linspace(0.5, 1.5, N))          # an all-positive column
+    X = rng.standard_normal((M, K))
+    X[:, rng.choice(K, 4, replace=False)] *= 35.0
+    return W, sq.f64_to_bf16(X), sq.f64_to_bf16(rng.standard_normal(N) * 0.1)
+
+
+def _nibbles(codes):
+    return np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
+
+
+def test_awq_host_quantiser_bit_exact_with_oracle_given_scales():
+    from oracle import awq
+    W, X, b = _awq_case(0)
+    s = (1.0 + np.random.default_rng(9).random(W.shape[1])).astype(np.float32)
+    o = svdq.awq_pack_host(W, bias=b, s=s)
+    p = awq.pack(W, b, s32=s)
+    assert np.array_equal(_nibbles(o["codes"]), p["codes"])
+    assert np.array_equal(o["scales"], p["scales"]) and np.array_equal(o["zeros"], p["zeros"])
+    assert np.array_equal(o["inv_s"], (np.float32(1.0) / s).astype(np.float32))
+    assert np.array_equal(o["bias"], b)
+
+
+def test_awq_host_search_matches_oracle():
+    from oracle import awq
+    W, X, b = _awq_case(1)
+    o = svdq.awq_pack_host(W, bias=b, Xcal=X)
+    p = awq.pack(W, b, Xcal_bits=X)
+    assert abs(o["alpha"] - p["alpha"]) < 1e-6
+    assert np.array_equal(o["s"], p["s"])
+    assert np.array_equal(_nibbles(o["codes"]), p["codes"])
+
+
+def test_awq_host_without_calibration_is_plain_rounding():
+    from oracle import awq
+    W, X, b = _awq_case(2)
+    o = svdq.awq_pack_host(W)
+    assert np.all(o["s"] == 1.0) and o["alpha"] == -1.0
+    q, sc, z = awq.quantize_groups(sq.bf16_to_f32(W))
+    assert np.array_equal(_nibbles(o["codes"]), q) and np.array_equal(o["scales"], sc)
+
+
+def test_awq_host_rejects_bad_shapes():
+    rng = np.random.default_rng(3)
+    W = sq.f64_to_bf16(rng.standard_normal((8, 96)))
+    with pytest.raises(svdq.SvdqError) as e:
+        svdq.awq_pack_host(W)                                    # K % 64 != 0
+    assert e.value.status == svdq.ERR_UNSUPPORTED_SHAPE

@@ -705,3 +705,133 @@ extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void
   if (e1 != 0) return cuda_fail(cudaError_t(e1), "kernel 1 launch");
   return launch_k2(h, a.x_codes, a.x_scales, a.T, Y, M, s);
 }
+
+// ------------------------------------------------------------------ AWQ-style W4A16 layer
+struct svdq_awq_layer {
+  AwqHostPack host;
+  int device = 0;
+  int sm_count = 0;
+  uint8_t* d_codes = nullptr;
+  float* d_scales = nullptr;
+  uint8_t* d_zeros = nullptr;
+  float* d_inv_s = nullptr;
+  uint16_t* d_bias = nullptr;
+};
+
+namespace {
+
+void free_awq(svdq_awq_layer* h) {
+  cudaFree(h->d_codes);
+  cudaFree(h->d_scales);
+  cudaFree(h->d_zeros);
+  cudaFree(h->d_inv_s);
+  cudaFree(h->d_bias);
+}
+
+void copy_awq_out(const AwqHostPack& hp, svdq_awq_host_t* out) {
+  const int64_t N = hp.N, K = hp.K, KG = K / 64;
+  if (out->s) std::memcpy(out->s, hp.s.data(), size_t(K) * 4);
+  if (out->inv_s) std::memcpy(out->inv_s, hp.inv_s.data(), size_t(K) * 4);
+  if (out->codes) std::memcpy(out->codes, hp.codes.data(), hp.codes.size());
+  if (out->scales) std::memcpy(out->scales, hp.scales.data(), size_t(N) * KG * 4);
+  if (out->zeros) std::memcpy(out->zeros, hp.zeros.data(), size_t(N) * KG);
+  if (out->bias_bf16) std::memcpy(out->bias_bf16, hp.bias.data(), size_t(N) * 2);
+  out->alpha = hp.alpha;
+}
+
+}  // namespace
+
+extern "C" {
+
+svdq_status_t svdq_awq_pack_host(const svdq_awq_params_t* p, svdq_awq_host_t* out) {
+  if (!p || !out) return fail(SVDQ_ERR_INVALID_ARG, "null argument");
+  AwqHostPack hp;
+  std::string err;
+  const svdq_status_t s = awq_pack_host(p, &hp, &err);
+  if (s != SVDQ_OK) return fail(s, err);
+  copy_awq_out(hp, out);
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_awq_pack(const svdq_awq_params_t* p, svdq_awq_handle_t* out) {
+  if (!p || !out) return fail(SVDQ_ERR_INVALID_ARG, "null argument");
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || p->device < 0 || p->device >= ndev)
+    return fail(SVDQ_ERR_INVALID_ARG, "no such device");
+  svdq_status_t s = check_arch(p->device);
+  if (s != SVDQ_OK) return s;
+  svdq_awq_layer* h = new (std::nothrow) svdq_awq_layer();
+  if (!h) return fail(SVDQ_ERR_OOM, "host allocation failed");
+  std::string err;
+  s = awq_pack_host(p, &h->host, &err);
+  if (s != SVDQ_OK) {
+    delete h;
+    return fail(s, err);
+  }
+  DeviceGuard guard(p->device);
+  h->device = p->device;
+  cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, p->device);
+  cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+  const AwqHostPack& hp = h->host;
+  auto up = [&](void** dst, const void* src, size_t bytes) -> cudaError_t {
+    cudaError_t ee;
+    *dst = dalloc(bytes, &ee);
+    if (ee != cudaSuccess) return ee;
+    if (bytes) ee = cudaMemcpyAsync(*dst, src, bytes, cudaMemcpyHostToDevice, stream);
+    return ee;
+  };
+  cudaError_t e = up(reinterpret_cast<void**>(&h->d_codes), hp.codes.data(), hp.codes.size());
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_scales), hp.scales.data(), hp.scales.size() * 4);
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_zeros), hp.zeros.data(), hp.zeros.size());
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_inv_s), hp.inv_s.data(), hp.inv_s.size() * 4);
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_bias), hp.bias.data(), hp.bias.size() * 2);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    free_awq(h);
+    delete h;
+    return e == cudaErrorMemoryAllocation ? fail(SVDQ_ERR_OOM, "device allocation failed")
+                                          : cuda_fail(e, "uploading the AWQ layer");
+  }
+  *out = h;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_awq_destroy(svdq_awq_handle_t h) {
+  if (!h) return SVDQ_OK;
+  DeviceGuard guard(h->device);
+  cudaDeviceSynchronize();
+  free_awq(h);
+  delete h;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_awq_export(svdq_awq_handle_t h, svdq_awq_host_t* out) {
+  if (!h || !out) return fail(SVDQ_ERR_INVALID_ARG, "null argument");
+  copy_awq_out(h->host, out);
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_awq_forward(svdq_awq_handle_t h, const void* X, void* Y, int64_t M, void* stream) {
+  if (!h || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M");
+  if (M == 0) return SVDQ_OK;
+  if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (X == Y) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not alias");
+  DeviceGuard guard(h->device);
+  AwqArgs a{};
+  a.X = static_cast<const uint16_t*>(X);
+  a.inv_s = h->d_inv_s;
+  a.codes = h->d_codes;
+  a.scales = h->d_scales;
+  a.zeros = h->d_zeros;
+  a.bias = h->d_bias;
+  a.Y = static_cast<uint16_t*>(Y);
+  a.M = M;
+  a.N = h->host.N;
+  a.K = h->host.K;
+  const int e = awq_launch(a, h->sm_count, stream);
+  if (e != 0) return cuda_fail(cudaError_t(e), "AWQ kernel launch");
+  return SVDQ_OK;
+}
+
+}  // extern "C"

@@ -31,6 +31,29 @@ struct HostPack {
 // Validates p and runs smoothing, SVD, residual and NVFP4 quantisation on the CPU.
 svdq_status_t pack_on_host(const svdq_pack_params_t* p, HostPack* out, std::string* err);
 
+// AWQ-style W4A16 layer: host pack (awq_host.cpp) and GEMV (awq_gemv.cu).
+struct AwqHostPack {
+  int64_t N = 0, K = 0;
+  float alpha = -1.f;
+  std::vector<float> s, inv_s;        // K
+  std::vector<uint8_t> codes;         // N x K/2
+  std::vector<float> scales;          // N x K/64
+  std::vector<uint8_t> zeros;         // N x K/64
+  std::vector<uint16_t> bias;         // N
+};
+svdq_status_t awq_pack_host(const svdq_awq_params_t* p, AwqHostPack* out, std::string* err);
+struct AwqArgs {
+  const uint16_t* X;                  // M x K bf16
+  const float* inv_s;                 // K
+  const uint8_t* codes;               // N x K/2
+  const float* scales;                // N x K/64
+  const uint8_t* zeros;               // N x K/64
+  const uint16_t* bias;               // N
+  uint16_t* Y;                        // M x N bf16
+  int64_t M, N, K;
+};
+int awq_launch(const AwqArgs& a, int sm_count, void* stream);
+
 // Activation-quantiser tables for a global scale s_g (host side):
 //   thr[c]  smallest float32 amax >= 0 whose block scale E4M3(fl32(amax / fl32(6 s_g))) >= c
 //           (c = 0..126; thr[127] = +inf), so the scale code of a block is the number of

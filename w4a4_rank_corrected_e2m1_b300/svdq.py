@@ -52,6 +52,20 @@ class Info(ctypes.Structure):
     ]
 
 
+class AwqParams(ctypes.Structure):
+    _fields_ = [
+        ("N", _i64), ("K", _i64), ("W_bf16", _vp), ("bias_bf16", _vp), ("Xcal_bf16", _vp), ("Mcal", _i64),
+        ("s", _vp), ("device", _i32), ("stream", _vp),
+    ]
+
+
+class AwqHost(ctypes.Structure):
+    _fields_ = [
+        ("s", _vp), ("inv_s", _vp), ("codes", _vp), ("scales", _vp), ("zeros", _vp), ("bias_bf16", _vp),
+        ("alpha", ctypes.c_float),
+    ]
+
+
 _SIGS = {
     "svdq_pack_host": (_i32, [ctypes.POINTER(PackParams), ctypes.POINTER(PackedHost)]),
     "svdq_pack_weights": (_i32, [ctypes.POINTER(PackParams), ctypes.POINTER(_vp)]),
@@ -68,6 +82,11 @@ _SIGS = {
     "svdq_linear_forward_host": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_check_error": (_i32, [_vp]),
     "svdq_attach_lora": (_i32, [_vp, _vp, _vp, _i64, ctypes.c_float, _vp]),
+    "svdq_awq_pack_host": (_i32, [ctypes.POINTER(AwqParams), ctypes.POINTER(AwqHost)]),
+    "svdq_awq_pack": (_i32, [ctypes.POINTER(AwqParams), ctypes.POINTER(_vp)]),
+    "svdq_awq_destroy": (_i32, [_vp]),
+    "svdq_awq_export": (_i32, [_vp, ctypes.POINTER(AwqHost)]),
+    "svdq_awq_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_status_string": (ctypes.c_char_p, [_i32]),
     "svdq_last_error": (ctypes.c_char_p, []),
 }
@@ -260,3 +279,65 @@ class Layer:
             raise ValueError(f"LoRA factors must be {self.K} x r and r x {self.N}")
         check(LIB.svdq_attach_lora(self.h, A.ctypes.data, B.ctypes.data, r_lora, float(scale), _stream(stream)),
               "svdq_attach_lora")
+
+
+# ------------------------------------------------------------------ AWQ-style W4A16 layer
+def _awq_params(W, bias=None, Xcal=None, s=None, device=0, stream=None):
+    W = _u16(W)
+    N, K = W.shape
+    bias = _u16(bias)
+    Xcal = _u16(Xcal)
+    s_arr = None if s is None else np.ascontiguousarray(s, dtype=np.float32)
+    p = AwqParams(N=N, K=K, W_bf16=W.ctypes.data, bias_bf16=None if bias is None else bias.ctypes.data,
+                  Xcal_bf16=None if Xcal is None else Xcal.ctypes.data, Mcal=0 if Xcal is None else Xcal.shape[0],
+                  s=None if s_arr is None else s_arr.ctypes.data, device=device, stream=_stream(stream))
+    return p, (W, bias, Xcal, s_arr)
+
+
+def _awq_out(N, K):
+    o = {"s": np.zeros(K, np.float32), "inv_s": np.zeros(K, np.float32), "codes": np.zeros((N, K // 2), np.uint8),
+         "scales": np.zeros((N, K // 64), np.float32), "zeros": np.zeros((N, K // 64), np.uint8),
+         "bias": np.zeros(N, np.uint16)}
+    st = AwqHost(s=o["s"].ctypes.data, inv_s=o["inv_s"].ctypes.data, codes=o["codes"].ctypes.data,
+                 scales=o["scales"].ctypes.data, zeros=o["zeros"].ctypes.data, bias_bf16=o["bias"].ctypes.data)
+    return o, st
+
+
+def awq_pack_host(W, bias=None, Xcal=None, s=None):
+    """Host quantisation of the AWQ-style layer; codes packed two per byte (low nibble first)."""
+    p, keep = _awq_params(W, bias, Xcal, s)
+    o, st = _awq_out(int(p.N), int(p.K))
+    check(LIB.svdq_awq_pack_host(ctypes.byref(p), ctypes.byref(st)), "svdq_awq_pack_host")
+    o["alpha"] = float(st.alpha)
+    return o
+
+
+class AwqLayer:
+    """A packed AWQ-style W4A16 layer on one CUDA device (wraps an svdq_awq_handle_t)."""
+
+    def __init__(self, W, bias=None, Xcal=None, s=None, device=0, stream=None):
+        p, keep = _awq_params(W, bias, Xcal, s, device, stream)
+        h = _vp()
+        check(LIB.svdq_awq_pack(ctypes.byref(p), ctypes.byref(h)), "svdq_awq_pack")
+        self.h = h
+        self.N, self.K = int(p.N), int(p.K)
+
+    def close(self):
+        if getattr(self, "h", None):
+            LIB.svdq_awq_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def export(self):
+        o, st = _awq_out(self.N, self.K)
+        check(LIB.svdq_awq_export(self.h, ctypes.byref(st)), "svdq_awq_export")
+        o["alpha"] = float(st.alpha)
+        return o
+
+    def forward(self, X, Y, M, stream=None):
+        check(LIB.svdq_awq_forward(self.h, _ptr(X), _ptr(Y), M, _stream(stream)), "svdq_awq_forward")

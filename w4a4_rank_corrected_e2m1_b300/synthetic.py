@@ -71,7 +71,14 @@ MLP_DOWN = Workload("flux_mlp_down", 4608, 12288, 3072, 32, x_kind="abs_student_
 OPROJ_M = [_flux(f"flux_oproj_m{m}", m, 3072, 3072, 32) for m in (256, 1024, 4096, 16384)]
 OPROJ_R = [_flux(f"flux_oproj_r{r}", 4096, 3072, 3072, r) for r in (16, 64, 128)]
 
-WORKLOADS: Dict[str, Workload] = {w.name: w for w in [TINY, QKV, MLP_UP, MLP_DOWN, *OPROJ_M, *OPROJ_R]}
+# AWQ-style W4A16 modulation layers: the conditioning vector (one row per image, two with
+# classifier-free guidance) against the adaptive-norm weight that produces the six
+# 3072-wide shift / scale / gate vectors of a FLUX double block; rank is unused (0)
+MOD = _flux("flux_mod", 1, 3072, 6 * 3072, 0)
+MOD_CFG = _flux("flux_mod_cfg", 2, 3072, 6 * 3072, 0)
+AWQ_WORKLOADS = [MOD, MOD_CFG]
+
+WORKLOADS: Dict[str, Workload] = {w.name: w for w in [TINY, QKV, MLP_UP, MLP_DOWN, *OPROJ_M, *OPROJ_R, *AWQ_WORKLOADS]}
 
 
 def get(name: str) -> Workload:
