@@ -260,8 +260,9 @@ const char* svdq_last_error(void);
  *   - activation-aware per-channel scales s_c = a_c^alpha / sqrt(max s * min s),
  *     a_c = mean_m |Xcal_mc|, alpha in {0, 0.05, ..., 0.95} picked by the smallest
  *     calibration output error (all ones without calibration data)
- *   - forward: x' = fl32(x * fl32(1 / s_c)), Y = x' ((q - z) sc)^T + b, float32 accumulation,
- *     bf16 out.  Built for the small-M (GEMV-like) modulation shapes: the weights are
+ *   - forward: x' = fl32(x * fl32(1 / s_c)), Y = x' ((q - z) sc)^T + b, bf16 out; the kernel
+ *     multiplies in fp16 (x' rounded to fp16) and sums eight products in fp16 before
+ *     float32, so |x'| must stay below 546.  Built for the small-M (GEMV-like) modulation shapes: the weights are
  *     streamed from HBM once per 8 rows of X.
  * ================================================================================== */
 typedef struct svdq_awq_layer* svdq_awq_handle_t;
@@ -300,6 +301,9 @@ svdq_status_t svdq_awq_export(svdq_awq_handle_t h, svdq_awq_host_t* out);
  * allocates nothing; X and Y 16-byte aligned, not aliased; M = 0 is a no-op.
  * Errors: INVALID_ARG, CUDA. */
 svdq_status_t svdq_awq_forward(svdq_awq_handle_t h, const void* X_bf16, void* Y_bf16, int64_t M, void* stream);
+/* Synchronises the layer's device, reads and clears its device error word: TIMEOUT if a
+ * kernel gave up a bounded wait since the last check. */
+svdq_status_t svdq_awq_check_error(svdq_awq_handle_t h);
 
 #ifdef __cplusplus
 }

@@ -26,6 +26,7 @@ def _run(layer, X, M):
     Y = torch.full((max(M, 1), layer.N), float("nan"), dtype=torch.bfloat16, device="cuda")
     layer.forward(Xd, Y, M)
     torch.cuda.synchronize()
+    layer.check_error()
     return sq.bf16_to_f64(gh.host_u16(Y.view(torch.int16)))[:M]
 
 

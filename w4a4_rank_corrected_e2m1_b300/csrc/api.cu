@@ -712,20 +712,20 @@ struct svdq_awq_layer {
   int device = 0;
   int sm_count = 0;
   uint8_t* d_codes = nullptr;
-  float* d_scales = nullptr;
-  uint8_t* d_zeros = nullptr;
+  float* d_sz = nullptr;            // N x K/64 (scale, zero point) pairs, 16 bytes of padding
   float* d_inv_s = nullptr;
   uint16_t* d_bias = nullptr;
+  int* d_err = nullptr;
 };
 
 namespace {
 
 void free_awq(svdq_awq_layer* h) {
   cudaFree(h->d_codes);
-  cudaFree(h->d_scales);
-  cudaFree(h->d_zeros);
+  cudaFree(h->d_sz);
   cudaFree(h->d_inv_s);
   cudaFree(h->d_bias);
+  cudaFree(h->d_err);
 }
 
 void copy_awq_out(const AwqHostPack& hp, svdq_awq_host_t* out) {
@@ -780,11 +780,19 @@ svdq_status_t svdq_awq_pack(const svdq_awq_params_t* p, svdq_awq_handle_t* out) 
     if (bytes) ee = cudaMemcpyAsync(*dst, src, bytes, cudaMemcpyHostToDevice, stream);
     return ee;
   };
+  std::vector<float> sz(hp.scales.size() * 2 + 4, 0.f);
+  for (size_t i = 0; i < hp.scales.size(); ++i) {
+    sz[2 * i] = hp.scales[i];
+    sz[2 * i + 1] = float(hp.zeros[i]);
+  }
   cudaError_t e = up(reinterpret_cast<void**>(&h->d_codes), hp.codes.data(), hp.codes.size());
-  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_scales), hp.scales.data(), hp.scales.size() * 4);
-  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_zeros), hp.zeros.data(), hp.zeros.size());
+  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_sz), sz.data(), sz.size() * 4);
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_inv_s), hp.inv_s.data(), hp.inv_s.size() * 4);
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_bias), hp.bias.data(), hp.bias.size() * 2);
+  if (e == cudaSuccess) {
+    h->d_err = static_cast<int*>(dalloc(sizeof(int), &e));
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->d_err, 0, sizeof(int), stream);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
     free_awq(h);
@@ -805,6 +813,19 @@ svdq_status_t svdq_awq_destroy(svdq_awq_handle_t h) {
   return SVDQ_OK;
 }
 
+svdq_status_t svdq_awq_check_error(svdq_awq_handle_t h) {
+  if (!h) return fail(SVDQ_ERR_INVALID_ARG, "null handle");
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronisation");
+  int v = 0;
+  e = cudaMemcpy(&v, h->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (v) return fail(SVDQ_ERR_TIMEOUT, "the AWQ kernel gave up a bounded wait");
+  return SVDQ_OK;
+}
+
 svdq_status_t svdq_awq_export(svdq_awq_handle_t h, svdq_awq_host_t* out) {
   if (!h || !out) return fail(SVDQ_ERR_INVALID_ARG, "null argument");
   copy_awq_out(h->host, out);
@@ -822,9 +843,9 @@ svdq_status_t svdq_awq_forward(svdq_awq_handle_t h, const void* X, void* Y, int6
   a.X = static_cast<const uint16_t*>(X);
   a.inv_s = h->d_inv_s;
   a.codes = h->d_codes;
-  a.scales = h->d_scales;
-  a.zeros = h->d_zeros;
+  a.sz = h->d_sz;
   a.bias = h->d_bias;
+  a.err = h->d_err;
   a.Y = static_cast<uint16_t*>(Y);
   a.M = M;
   a.N = h->host.N;

@@ -5,20 +5,26 @@
 // weights (aiflownews article on Nunchaku, "How Nunchaku four bit quantization actually
 // works").
 //
-// The work is one pass over the packed weights (HBM-bound: 0.5 byte per weight plus 5 bytes
-// per group), so the design keeps the ALU cost per weight small:
-//   * the block's rows of x' sit in shared memory in 32-element segments padded by 4 floats,
-//     so the eight 16-byte reads a lane makes for its 32 channels are conflict-free;
-//   * a lane takes 16 bytes of codes (32 weights, half a group) at a time and turns a code q
-//     into the exact float 1 + q/16 with one shift and one LOP3 (exponent of 1.0, q in the
-//     top mantissa bits); two products accumulate per packed fma.rn.f32x2;
-//   * the zero point and scale are applied once per 32 weights through
-//       sum_k x'_k (q_k - z) = 16 sum_k x'_k (1 + q_k/16) - (16 + z) sum_k x'_k,
-//     with the 32-channel sums of x' precomputed per block;
-//   * each warp owns whole output rows (grid-strided), reduces its lanes with shuffles and
-//     writes bf16(acc + b).
-// Codes are read with non-allocating 16-byte loads; a warp issues all of two rows' loads (up
-// to four per lane per row) before using any.
+// The work is one pass over the packed weights (HBM-bound: 0.5 byte per weight plus 8 bytes
+// per group of 64), streamed by one block per SM: a producer warp moves the block's
+// contiguous run of weight rows (codes, then the rows' (scale, zero point) pairs) through a
+// shared-memory ring with bulk copies, and sixteen warps consume it (one weight row each per
+// stage), keeping the ALU cost per
+// weight small:
+//   * the block's rows of x' sit in shared memory in fp16, 32-channel segments padded to 80
+//     bytes so that a warp's 16-byte reads are conflict-free;
+//   * a lane takes 16 bytes of codes (32 weights, half a group) at a time; LOP3s turn two codes
+//     into the fp16 pair (1024 + q) (or (1024 + 16 q) for the odd nibbles, which need no
+//     shift), one HSUB2 subtracts (1024 + z) or (1024 + 16 z) (exact: the differences are small
+//     integers), and HFMA2 multiplies by the paired x' values;
+//   * two 16-byte words' products (eight per half) are summed in fp16 and added into a float32
+//     total, which the group scale multiplies once per 32 weights;
+//   * the warp reduces its lanes with shuffles and writes bf16(acc + b).
+// fp16 keeps 11 bits of the products (|x'| must stay below 65504 / (8 * 15) for the sums of
+// eight products); longer sums are float32.
+// Every wait is bounded (about two seconds; on expiry the error word is set and the block
+// returns).
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -28,141 +34,261 @@ namespace svdq {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;              // compute warps (a producer warp comes on top)
 constexpr int kWarps = kThreads / 32;
 
-__host__ __device__ constexpr int64_t padded(int64_t k) { return k + (k >> 5) * 4; }   // 32 floats + 4 pad
+// x' is kept in fp16 in shared memory, one 80-byte slot per 32-channel segment (64 bytes of
+// data, 16 of padding so that the four 16-byte reads of a warp quarter hit distinct banks).
+// Inside a segment, word u (channels 8u .. 8u + 7) holds the pairs (8u + p, 8u + p + 4),
+// p = 0..3, matching the order in which one LOP3 pulls two codes out of a 32-bit word.
+constexpr int kSegBytes = 80;
+__host__ __device__ constexpr int64_t xs_bytes_per_row(int64_t K) { return (K / 32) * kSegBytes; }
 
-__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
-  uint64_t d, x, y, z;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(z) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
-  return r;
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+// Bounded mbarrier wait: about two seconds, then the block gives up (flag + error word).
+__device__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
 }
 
-// 1 + q/16 for nibble i of w (exact: exponent of 1.0, q in mantissa bits 22..19)
-template <int I>
-__device__ __forceinline__ float nib(uint32_t w) {
-  constexpr int sh = 4 * I - 19;
-  const uint32_t v = sh >= 0 ? (w >> sh) : (w << -sh);
-  return __uint_as_float((v & 0x00780000u) | 0x3F800000u);
+// Two codes of a 32-bit word as fp16 (1024 + q): nibbles at bits 4p and 4p + 16 go into the
+// low and high mantissas of the exponent of 1024 (one LOP3 after the shift).
+template <int P>
+__device__ __forceinline__ __half2 codes_pair(uint32_t w) {
+  uint32_t v = (w >> (4 * P)) & 0x000F000Fu;
+  v |= 0x64006400u;
+  return *reinterpret_cast<__half2*>(&v);
+}
+
+// Rows per stage and ring depth for a K (codes 0.5 B and scale/zero pairs 8 B / 64 per weight)
+struct AwqPlan {
+  int rs, stages, mb;
+  size_t stage_bytes, xs_bytes, smem;
+};
+
+__host__ __device__ constexpr int64_t stage_rows_for(int64_t K) { return K <= 6144 ? 16 : (K <= 12288 ? 8 : 4); }
+
+__device__ __forceinline__ unsigned char* xs_row(unsigned char* xs, int m, int64_t K) {
+  return xs + size_t(m) * xs_bytes_per_row(K);
 }
 
 template <int MB>
-__global__ void __launch_bounds__(kThreads) awq_gemv_kernel(AwqArgs a, int64_t m0) {
-  extern __shared__ __align__(16) float sm[];
+__global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, int64_t m0, int rs, int stages,
+                                                                   int stage_bytes) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ uint64_t full[8], empty[8];
+  __shared__ volatile int abort_flag;
   const int64_t K = a.K, N = a.N;
-  const int64_t KP = padded(K);
   const int nseg = int(K / 32);
-  float* xs = sm;                       // [MB][KP]: x' in padded 32-float segments
-  float* seg_sum = sm + MB * KP;        // [MB][K / 32]: sum of each segment of x'
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-#pragma unroll
-  for (int m = 0; m < MB; ++m) {
-    const bool live = m0 + m < a.M;
-    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
-      float v = 0.f;
-      if (live) v = __fmul_rn(__uint_as_float(uint32_t(a.X[(m0 + m) * K + k]) << 16), a.inv_s[k]);
-      xs[m * KP + padded(k)] = v;
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < MB * nseg; i += blockDim.x) {
-    const int m = i / nseg, sgi = i - m * nseg;
-    const float* p = xs + m * KP + int64_t(sgi) * 36;
-    float s = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) s += p[j];
-    seg_sum[m * nseg + sgi] = s;
-  }
-  __syncthreads();
-
   const int64_t KG = K / 64;
-  const int64_t nwarps = int64_t(gridDim.x) * kWarps;
-  // two output rows per warp at a time, and up to kBatch 16-byte code loads per row per lane
-  // issued before any of them is used, so that enough bytes are in flight to cover HBM latency
-  constexpr int kRowsInFlight = 2, kBatch = 4;
-  for (int64_t n0 = int64_t(blockIdx.x) * kWarps + warp; n0 < N; n0 += nwarps * kRowsInFlight) {
-    float part[kRowsInFlight][MB];
-#pragma unroll
-    for (int r = 0; r < kRowsInFlight; ++r)
-#pragma unroll
-      for (int m = 0; m < MB; ++m) part[r][m] = 0.f;
-    for (int sb = 0; sb < nseg; sb += 32 * kBatch) {
-      uint4 c[kRowsInFlight][kBatch];
-      float sc[kRowsInFlight][kBatch], zf[kRowsInFlight][kBatch];
-#pragma unroll
-      for (int r = 0; r < kRowsInFlight; ++r) {
-        const int64_t n = n0 + r * nwarps;
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-          const int sgi = sb + lane + 32 * i;
-          if (n < N && sgi < nseg) {
-            c[r][i] = ptx::ld_stream_v4(a.codes + n * (K / 2) + int64_t(sgi) * 16);
-            sc[r][i] = __ldg(a.scales + n * KG + (sgi >> 1));
-            zf[r][i] = float(__ldg(a.zeros + n * KG + (sgi >> 1)));
-          } else {
-            c[r][i] = make_uint4(0, 0, 0, 0);
-            sc[r][i] = 0.f;
-            zf[r][i] = 0.f;
-          }
+  unsigned char* xs = smem_raw;                                     // [MB] rows of x' (fp16, paired segments)
+  unsigned char* ring = smem_raw + ((size_t(MB) * xs_bytes_per_row(K) + 127) / 128) * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int codes_row = int(K / 2), sz_row = int(KG * 8);
+
+  // rows [r_begin, r_end) of this block: a contiguous run of the packed weights
+  const int64_t per_block = ((N + gridDim.x - 1) / gridDim.x + rs - 1) / rs * rs;
+  const int64_t r_begin = int64_t(blockIdx.x) * per_block;
+  const int64_t r_end = r_begin + per_block < N ? r_begin + per_block : N;
+  const int nst = r_begin < r_end ? int((r_end - r_begin + rs - 1) / rs) : 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], kWarps);
+    }
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ------------------------------------------------------------ producer (bulk copies)
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int j = 0; j < nst; ++j, ++issued) {
+        if (j >= stages) {
+          if (!bounded_wait(&empty[stage], phase ^ 1u, &abort_flag)) break;
+          ptx::fence_proxy_async_smem();   // the compute warps' ordinary loads before the refill
         }
+        const int64_t row = r_begin + int64_t(j) * rs;
+        const int nrows = int(r_end - row < rs ? r_end - row : rs);
+        unsigned char* st = ring + size_t(stage) * stage_bytes;
+        // the pair copy is rounded up to 16 bytes (the device array carries 16 bytes of padding)
+        const uint32_t cb = uint32_t(nrows * codes_row), zb = (uint32_t(nrows * sz_row) + 15u) & ~15u;
+        ptx::mbar_arrive_expect_tx(&full[stage], cb + zb);
+        ptx::bulk_load(st, a.codes + row * codes_row, cb, &full[stage]);
+        ptx::bulk_load(st + size_t(rs) * codes_row, reinterpret_cast<const unsigned char*>(a.sz) + row * sz_row, zb,
+                       &full[stage]);
+        if (++stage == stages) { stage = 0; phase ^= 1u; }
       }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int sgi = sb + lane + 32 * i;
-        if (sgi >= nseg) break;
-#pragma unroll
-        for (int m = 0; m < MB; ++m) {
-          const float4* xp = reinterpret_cast<const float4*>(xs + m * KP + int64_t(sgi) * 36);
-          float4 xv[8];
-#pragma unroll
-          for (int v = 0; v < 8; ++v) xv[v] = xp[v];                  // channels 4v .. 4v + 3
-          const float ssum = seg_sum[m * nseg + sgi];
-#pragma unroll
-          for (int r = 0; r < kRowsInFlight; ++r) {
-            float2 acc = make_float2(0.f, 0.f);
-            const uint32_t cw[4] = {c[r][i].x, c[r][i].y, c[r][i].z, c[r][i].w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {                              // channels 8u .. 8u + 7
-              const uint32_t w = cw[u];                                // element 2j in the low nibble
-              const float4 x0 = xv[2 * u], x1 = xv[2 * u + 1];
-              acc = fma2_rn(make_float2(x0.x, x0.y), make_float2(nib<0>(w), nib<1>(w)), acc);
-              acc = fma2_rn(make_float2(x0.z, x0.w), make_float2(nib<2>(w), nib<3>(w)), acc);
-              acc = fma2_rn(make_float2(x1.x, x1.y), make_float2(nib<4>(w), nib<5>(w)), acc);
-              acc = fma2_rn(make_float2(x1.z, x1.w), make_float2(nib<6>(w), nib<7>(w)), acc);
-            }
-            const float t = acc.x + acc.y;                             // sum x' (1 + q/16)
-            part[r][m] = fmaf(sc[r][i], fmaf(16.f, t, -(16.f + zf[r][i]) * ssum), part[r][m]);
-          }
-        }
+      for (int i = 0; i < stages; ++i) {       // every copy issued has landed
+        const int used = issued - i;
+        if (used <= 0) continue;
+        bounded_wait(&full[i], uint32_t(((used - 1) / stages) & 1), &abort_flag);
       }
     }
+  } else {
+    // ------------------------------------------------------------ compute warps
+    // x' = fl32(x * fl32(1 / s)) rounded to fp16, in the paired segment order: a thread takes 8
+    // channels (one 16-byte load of X) and writes them as one 16-byte word of a segment
+    for (int64_t k8 = threadIdx.x; k8 < K / 8; k8 += kThreads) {
+      const int64_t k = 8 * k8;
+      const float4 i0 = *reinterpret_cast<const float4*>(a.inv_s + k);
+      const float4 i1 = *reinterpret_cast<const float4*>(a.inv_s + k + 4);
+      const float inv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+      uint4 xr[MB];
 #pragma unroll
-    for (int r = 0; r < kRowsInFlight; ++r) {
-      const int64_t n = n0 + r * nwarps;
+      for (int m = 0; m < MB; ++m)
+        xr[m] = m0 + m < a.M ? *reinterpret_cast<const uint4*>(a.X + (m0 + m) * K + k) : make_uint4(0, 0, 0, 0);
+      const int64_t sgi = k >> 5;
+      const int u = int(k & 31) >> 3;
 #pragma unroll
       for (int m = 0; m < MB; ++m) {
-        float v = part[r][m];
+        const uint32_t xw[4] = {xr[m].x, xr[m].y, xr[m].z, xr[m].w};
+        float v[8];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        if (lane == 0 && n < N && m0 + m < a.M) {
-          const float b = __uint_as_float(uint32_t(a.bias[n]) << 16);
-          a.Y[(m0 + m) * N + n] = uint16_t(ptx::pack_bf16x2(v + b, 0.f) & 0xFFFFu);
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t bits = (e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16);
+          v[e] = __fmul_rn(__uint_as_float(bits), inv[e]);
         }
+        // pairs (e, e + 4), e = 0..3; the odd pairs meet codes read as 16 q, so they are stored
+        // divided by 16 (exact power-of-two scaling) to keep every product x' (q - z)
+        uint4 out;
+        __half2 h;
+        h = __floats2half2_rn(v[0], v[4]); out.x = *reinterpret_cast<uint32_t*>(&h);
+        h = __floats2half2_rn(0.0625f * v[1], 0.0625f * v[5]); out.y = *reinterpret_cast<uint32_t*>(&h);
+        h = __floats2half2_rn(v[2], v[6]); out.z = *reinterpret_cast<uint32_t*>(&h);
+        h = __floats2half2_rn(0.0625f * v[3], 0.0625f * v[7]); out.w = *reinterpret_cast<uint32_t*>(&h);
+        *reinterpret_cast<uint4*>(xs_row(xs, m, K) + sgi * kSegBytes + u * 16) = out;
       }
     }
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads));
+
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < nst; ++j) {
+      if (!bounded_wait(&full[stage], phase, &abort_flag)) break;
+      const unsigned char* st = ring + size_t(stage) * stage_bytes;
+      const int64_t row0 = r_begin + int64_t(j) * rs;
+      for (int rr = warp; rr < rs; rr += kWarps) {
+        const int64_t n = row0 + rr;
+        if (n >= r_end) break;
+        const uint32_t crow = ptx::smem_u32(st + size_t(rr) * codes_row);
+        const uint32_t szrow = ptx::smem_u32(st + size_t(rs) * codes_row + size_t(rr) * sz_row);
+        float part[MB];
+#pragma unroll
+        for (int m = 0; m < MB; ++m) part[m] = 0.f;
+        // three 32-weight chunks per lane at a time (K = 3072 in one pass), all loaded first
+        constexpr int kU = 3;
+        for (int sg0 = lane; sg0 < nseg; sg0 += 32 * kU) {
+          uint4 c[kU];
+          float2 sz[kU];
+#pragma unroll
+          for (int i = 0; i < kU; ++i) {
+            const int sgi = sg0 + 32 * i;
+            if (sgi < nseg) {
+              c[i] = ptx::lds_v4(crow + uint32_t(sgi) * 16u);
+              sz[i] = ptx::lds_f32x2(szrow + uint32_t(sgi >> 1) * 8u);    // scale, zero point
+            } else {
+              c[i] = make_uint4(0x64646464u, 0x64646464u, 0x64646464u, 0x64646464u);
+              sz[i] = make_float2(0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kU; ++i) {
+            const int sgi = sg0 + 32 * i;
+            // codes 8u + p (low half) and 8u + p + 4 (high half): for p = 0, 2 as fp16 (1024 + q),
+            // for p = 1, 3 straight from bits 4..7 as (1024 + 16 q) (exact: multiples of 16 below
+            // 1024); subtracting (1024 + z), resp. (1024 + 16 z), leaves q - z, resp. 16 (q - z)
+            const __half2 zz = __float2half2_rn(1024.f + sz[i].y);
+            const __half2 zz16 = __float2half2_rn(1024.f + 16.f * sz[i].y);
+            const uint32_t cw[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
+            __half2 qz[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t w = cw[u], w8 = cw[u] >> 8;
+              uint32_t v0 = (w & 0x000F000Fu) | 0x64006400u, v1 = (w & 0x00F000F0u) | 0x64006400u;
+              uint32_t v2 = (w8 & 0x000F000Fu) | 0x64006400u, v3 = (w8 & 0x00F000F0u) | 0x64006400u;
+              qz[u][0] = __hsub2(*reinterpret_cast<__half2*>(&v0), zz);
+              qz[u][1] = __hsub2(*reinterpret_cast<__half2*>(&v1), zz16);
+              qz[u][2] = __hsub2(*reinterpret_cast<__half2*>(&v2), zz);
+              qz[u][3] = __hsub2(*reinterpret_cast<__half2*>(&v3), zz16);
+            }
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+              const uint32_t xp = ptx::smem_u32(xs_row(xs, m, K)) + uint32_t(sgi < nseg ? sgi : 0) * kSegBytes;
+              // products of pairs 0, 2 and of pairs 1, 3 in two fp16 sums per two words (eight
+              // products per half), then float32
+              float t = 0.f;
+#pragma unroll
+              for (int uu = 0; uu < 4; uu += 2) {
+                const uint4 xa = ptx::lds_v4(xp + 16u * uu), xb = ptx::lds_v4(xp + 16u * (uu + 1));
+                __half2 e = __hmul2(*reinterpret_cast<const __half2*>(&xa.x), qz[uu][0]);
+                e = __hfma2(*reinterpret_cast<const __half2*>(&xa.z), qz[uu][2], e);
+                e = __hfma2(*reinterpret_cast<const __half2*>(&xb.x), qz[uu + 1][0], e);
+                e = __hfma2(*reinterpret_cast<const __half2*>(&xb.z), qz[uu + 1][2], e);
+                __half2 o = __hmul2(*reinterpret_cast<const __half2*>(&xa.y), qz[uu][1]);
+                o = __hfma2(*reinterpret_cast<const __half2*>(&xa.w), qz[uu][3], o);
+                o = __hfma2(*reinterpret_cast<const __half2*>(&xb.y), qz[uu + 1][1], o);
+                o = __hfma2(*reinterpret_cast<const __half2*>(&xb.w), qz[uu + 1][3], o);
+                const float2 fe = __half22float2(e), fo = __half22float2(o);
+                t += (fe.x + fe.y) + (fo.x + fo.y);
+              }
+              part[m] = fmaf(sz[i].x, t, part[m]);                 // sum x' (q - z) * sc
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+          float v = part[m];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+          if (lane == 0 && m0 + m < a.M) {
+            const float b = __uint_as_float(uint32_t(a.bias[n]) << 16);
+            a.Y[(m0 + m) * N + n] = uint16_t(ptx::pack_bf16x2(v + b, 0.f) & 0xFFFFu);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[stage]);
+      if (++stage == stages) { stage = 0; phase ^= 1u; }
+    }
   }
+  if (abort_flag && threadIdx.x == 0) atomicOr(a.err, 16);
+}
+
+AwqPlan awq_plan(int64_t K, int64_t M) {
+  AwqPlan p{};
+  p.rs = int(stage_rows_for(K));
+  p.stage_bytes = ((size_t(p.rs) * (K / 2 + (K / 64) * 8)) + 16 + 127) / 128 * 128;
+  p.mb = M >= 8 ? 8 : (M >= 4 ? 4 : (M >= 2 ? 2 : 1));
+  for (;; p.mb >>= 1) {
+    p.xs_bytes = (size_t(p.mb) * xs_bytes_per_row(K) + 127) / 128 * 128;
+    const size_t room = size_t(210) * 1024 > p.xs_bytes ? size_t(210) * 1024 - p.xs_bytes : 0;
+    p.stages = int(room / p.stage_bytes);
+    if (p.stages > 8) p.stages = 8;
+    if (p.stages >= 3 || p.mb == 1) break;
+  }
+  p.smem = p.xs_bytes + size_t(p.stages) * p.stage_bytes;
+  return p;
 }
 
 template <int MB>
-int launch_mb(const AwqArgs& a, int sm_count, cudaStream_t s) {
-  const size_t smem = (size_t(MB) * padded(a.K) + size_t(MB) * (a.K / 32)) * sizeof(float);
+int launch_mb(const AwqArgs& a, const AwqPlan& p, int sm_count, cudaStream_t s) {
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -171,12 +297,10 @@ int launch_mb(const AwqArgs& a, int sm_count, cudaStream_t s) {
     if (e != cudaSuccess) return int(e);
     attr_done[dev] = 1;
   }
-  const int64_t rows_per_block = kWarps;
-  int64_t blocks = (a.N + rows_per_block - 1) / rows_per_block;
-  const int64_t cap = int64_t(sm_count) * (smem <= 100 * 1024 ? 2 : 1) * 2;   // a couple of waves of rows each
-  if (blocks > cap) blocks = cap;
+  // one block per SM, each streaming a contiguous run of rows
+  const int64_t blocks = sm_count < a.N ? sm_count : a.N;
   for (int64_t m0 = 0; m0 < a.M; m0 += MB) {
-    awq_gemv_kernel<MB><<<unsigned(blocks), kThreads, smem, s>>>(a, m0);
+    awq_gemv_kernel<MB><<<unsigned(blocks), kThreads + 32, p.smem, s>>>(a, m0, p.rs, p.stages, int(p.stage_bytes));
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return int(e);
   }
@@ -185,19 +309,15 @@ int launch_mb(const AwqArgs& a, int sm_count, cudaStream_t s) {
 
 }  // namespace
 
-size_t awq_smem_bytes(int64_t K, int mb) { return (size_t(mb) * padded(K) + size_t(mb) * (K / 32)) * sizeof(float); }
-
 int awq_launch(const AwqArgs& a, int sm_count, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // rows of X per pass: as many as the shared memory for x' allows, at most 8
-  int mb = a.M >= 8 ? 8 : (a.M >= 4 ? 4 : (a.M >= 2 ? 2 : 1));
-  while (mb > 1 && awq_smem_bytes(a.K, mb) > 200 * 1024) mb >>= 1;
-  if (awq_smem_bytes(a.K, mb) > 200 * 1024) return int(cudaErrorInvalidValue);
-  switch (mb) {
-    case 8: return launch_mb<8>(a, sm_count, s);
-    case 4: return launch_mb<4>(a, sm_count, s);
-    case 2: return launch_mb<2>(a, sm_count, s);
-    default: return launch_mb<1>(a, sm_count, s);
+  const AwqPlan p = awq_plan(a.K, a.M);
+  if (p.stages < 2) return int(cudaErrorInvalidValue);
+  switch (p.mb) {
+    case 8: return launch_mb<8>(a, p, sm_count, s);
+    case 4: return launch_mb<4>(a, p, sm_count, s);
+    case 2: return launch_mb<2>(a, p, sm_count, s);
+    default: return launch_mb<1>(a, p, sm_count, s);
   }
 }
 

@@ -46,10 +46,10 @@ struct AwqArgs {
   const uint16_t* X;                  // M x K bf16
   const float* inv_s;                 // K
   const uint8_t* codes;               // N x K/2
-  const float* scales;                // N x K/64
-  const uint8_t* zeros;               // N x K/64
+  const float* sz;                    // N x K/64 pairs (scale, zero point as float), 16 bytes of padding
   const uint16_t* bias;               // N
   uint16_t* Y;                        // M x N bf16
+  int* err;                           // device error word (bounded waits)
   int64_t M, N, K;
 };
 int awq_launch(const AwqArgs& a, int sm_count, void* stream);

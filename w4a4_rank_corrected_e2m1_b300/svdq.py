@@ -87,6 +87,7 @@ _SIGS = {
     "svdq_awq_destroy": (_i32, [_vp]),
     "svdq_awq_export": (_i32, [_vp, ctypes.POINTER(AwqHost)]),
     "svdq_awq_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
+    "svdq_awq_check_error": (_i32, [_vp]),
     "svdq_status_string": (ctypes.c_char_p, [_i32]),
     "svdq_last_error": (ctypes.c_char_p, []),
 }
@@ -341,3 +342,6 @@ class AwqLayer:
 
     def forward(self, X, Y, M, stream=None):
         check(LIB.svdq_awq_forward(self.h, _ptr(X), _ptr(Y), M, _stream(stream)), "svdq_awq_forward")
+
+    def check_error(self):
+        check(LIB.svdq_awq_check_error(self.h), "svdq_awq_check_error")
