@@ -38,12 +38,14 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on 
 # captures summarised under profiles/, keyed by the workload and by a hash of the kernel's
 # sources at capture time: a kernel edited since then reports null traffic.
 NCU_TRAFFIC = {
-    ("flux_mlp_up", "k1_actquant"): ("bf09ba97012e1cec", 28.549632e6 + 0.025344e6),
-    ("flux_mlp_up", "k2_fp4gemm"): ("594f6e9e8c533bfc", 33.080064e6 + 63.747072e6),
+    ("flux_mlp_up", "k1_actquant"): ("a6ec7f325c0acea1", 28.553216e6 + 0.0),
+    ("flux_mlp_up", "k2_fp4gemm"): ("da0881e7e67757fd", 33.013248e6 + 64.824320e6),
+    ("flux_mod", "awq_gemv"): ("b38f04e463acbbf2", 35.471872e6 + 0.0),
 }
 KERNEL_SOURCES = {
     "k1_actquant": ["k1_actquant.cu", "ptx.cuh", "svdq_internal.h"],
     "k2_fp4gemm": ["k2_fp4gemm.cu", "ptx.cuh", "svdq_internal.h"],
+    "awq_gemv": ["awq_gemv.cu", "ptx.cuh", "svdq_internal.h"],
 }
 
 
@@ -413,11 +415,114 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ AWQ-style W4A16 layer
+AWQ_METRIC = "AWQ-style W4A16 linear at the FLUX modulation shape: packed-weight GB/s and tokens/s"
+
+
+def awq_bytes(w):
+    """Algorithmic HBM bytes of one forward: codes, (scale, zero) pairs, 1/s, bias, X, Y."""
+    return w.N * w.K / 2 + w.N * (w.K // 64) * 8 + w.K * 4 + w.N * 2 + w.M * w.K * 2 + w.M * w.N * 2
+
+
+def run_awq(args, w):
+    """The modulation layers' weight-only 4-bit linear (its own JSON line; replicas like the main
+    layer under torchrun)."""
+    import torch
+    import torch.distributed as dist
+    from w4a4_rank_corrected_e2m1_b300 import svdq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    d = synthetic.make(w)
+    layer = svdq.AwqLayer(d["W"], bias=d["bias"], Xcal=synthetic.make_x(w, 64, seed=7), device=local)
+    stream = torch.cuda.current_stream()
+    Xs = [torch.from_numpy(synthetic.make_x(w, w.M, seed=sd).view(np.int16)).cuda() for sd in batch_seeds(rank, 4)]
+    Y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for i in range(args.warmup):
+        layer.forward(Xs[i % 4], Y, w.M, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = Clocks(torch.cuda.current_device())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        layer.forward(Xs[i % 4], Y, w.M, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    layer.check_error()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    (ms,) = max_over_ranks([ms], world, "cuda")
+    if rank == 0:
+        hbm, _, src = peaks()
+        by = awq_bytes(w)
+        gbs = job_rate(by, world, ms * 1e-3) / 1e9
+        per_gpu = by / (ms * 1e-3) / 1e9
+        out = {
+            "metric": AWQ_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u4 weights (group 64, f32 scale, zero point) x bf16 acts; f16 products, f32 sums",
+            "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "group": 64,
+                       "l2": "flushed before every timed step (256 MiB write outside the timed events)",
+                       "parallelism": f"replicas x{world}"},
+            "tokens_per_s": job_rate(w.M, world, ms * 1e-3),
+            "roofline": {"bound": "hbm", "kernel": "awq_gemv", "achieved": per_gpu, "peak": hbm, "unit": "GB/s",
+                         "frac": per_gpu / hbm, "traffic": ncu_traffic(w.name, "awq_gemv"),
+                         "traffic_unit": "bytes per launch (ncu)", "algorithmic_bytes": by,
+                         "peak_source": f"{src} copy bandwidth"},
+            "gpu_launches": args.steps * ((w.M + 7) // 8), "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+    layer.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_awq(args, w):
+    """The AWQ oracle's forward on the host cores (weights quantised once, without the scale
+    search, which does not change the forward's cost)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from oracle import awq
+    d = synthetic.make(w)
+    p = awq.pack(d["W"], d["bias"])
+    for _ in range(min(args.warmup, 1)):
+        awq.forward(d["X"], p)
+    steps = max(1, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        awq.forward(d["X"], p)
+    dt = (time.perf_counter() - t0) / steps
+    val = awq_bytes(w) / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": AWQ_METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "group": 64},
+        "tokens_per_s": w.M / dt,
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": len(os.sched_getaffinity(0)), "threads": blas_threads(),
+                         "kind": "oracle", "sample": f"oracle AWQ forward, {steps} steps of {w.M} rows"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     args = parse()
     w = synthetic.get(args.workload)
     if args.impl == "reference":
-        run_reference(args, w)
+        if w in synthetic.AWQ_WORKLOADS:
+            run_reference_awq(args, w)
+        else:
+            run_reference(args, w)
+    elif w in synthetic.AWQ_WORKLOADS:
+        run_awq(args, w)
     else:
         run_ours(args, w)
 
