@@ -278,10 +278,12 @@ def test_ragged_n_and_k():
     gh.assert_y_close(Y, sq.forward(d["X"], gh.oracle_packed(exp)), "ragged")
 
 
-def test_tall_path_ragged_m_and_odd_chunk_count():
+@pytest.mark.parametrize("rank", [16, 32, 48, 64, 96])
+def test_tall_path_ragged_m_and_odd_chunk_count(rank):
     """M large enough for the whole-K 32-row kernel, M % 32 != 0, K with an odd number of
-    64-column chunks (the last stage's second chunk is past K) and K % 256 != 0."""
-    w = synthetic.scaled(synthetic.QKV, name="tall_ragged", M=2413, K=576, N=256, rank=32, n_outlier=6)
+    64-column chunks (the last stage's later chunks are past K) and K % 256 != 0; ranks on
+    both down-projection forms (four chunks in one product for r <= 64, one per chunk above)."""
+    w = synthetic.scaled(synthetic.QKV, name="tall_ragged", M=2413, K=576, N=256, rank=rank, n_outlier=6)
     d, layer, exp = case(w)
     c, s, t, raw = run_k1(layer, d["X"], w.M)
     rc, rs, xh = sq.quantize_act(d["X"], exp["inv_lambda"], exp["s_gX"])
@@ -297,12 +299,13 @@ def test_tall_path_ragged_m_and_odd_chunk_count():
     gh.assert_y_close(Y, sq.forward(d["X"], gh.oracle_packed(exp)), "tall ragged")
 
 
-@pytest.mark.parametrize("w", [synthetic.QKV, synthetic.OPROJ_M[1]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [synthetic.QKV, synthetic.scaled(synthetic.MLP_DOWN, name="down_m1024", M=1024)],
+                         ids=lambda w: w.name)
 def test_k1_bitexact_on_repeated_launches(w):
-    """Kernel 1 run back to back (whole-K 32-row kernel for QKV, split-K kernel for the
-    1024-token o-proj): every launch is bit-exact.  A missing ordering between the
-    quantiser's reads of a stage and the copies that refill it shows up here as a few
-    blocks read from the wrong step."""
+    """Kernel 1 run back to back (whole-K 32-row kernel for QKV, split-K kernel for 1024
+    tokens of the MLP down-projection, K = 12288): every launch is bit-exact.  A missing
+    ordering between the quantiser's reads of a stage and the copies that refill it shows up
+    here as a few blocks read from the wrong step."""
     d, layer, exp = case(w)
     rc, rs, _ = sq.quantize_act(d["X"], exp["inv_lambda"], exp["s_gX"])
     for i in range(6):

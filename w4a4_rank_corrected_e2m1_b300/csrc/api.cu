@@ -209,7 +209,13 @@ svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
         const int unit = (i / 8) ^ int(j % 8);
         reinterpret_cast<uint16_t*>(slice + j * 128 + unit * 16)[i % 8] = v;
       }
-    std::memcpy(grp + 4 * rk * 128 + (c % 4) * 256, hp.inv_lambda.data() + 64 * c, 256);
+    // 1/lambda part: thread t of a quantiser quad reads floats 16 t .. 16 t + 15 as four 16-byte
+    // loads k = 0..3; load k of thread t sits in 16-byte unit 4 t + (k ^ (t >> 1)), so the four
+    // threads' k-th loads fall in four different bank groups
+    for (int tt = 0; tt < 4; ++tt)
+      for (int kk = 0; kk < 4; ++kk)
+        std::memcpy(grp + 4 * rk * 128 + (c % 4) * 256 + 16 * (4 * tt + (kk ^ (tt >> 1))),
+                    hp.inv_lambda.data() + 64 * c + 16 * tt + 4 * kk, 16);
   }
   cudaError_t e;
   uint16_t* d_l2t = static_cast<uint16_t*>(dalloc(l2t.size() * 2, &e));

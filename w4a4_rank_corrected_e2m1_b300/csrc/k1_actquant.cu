@@ -96,27 +96,31 @@ __device__ __forceinline__ void li_loads(unsigned char* st, const unsigned char*
 // Returns s8 and the 16 codes as two words (element 2j in the low nibble of byte j).
 __device__ __forceinline__ uint32_t quant_block(const uint32_t* w, const float* il, float inv_six, const float* s_thr,
                                                 const float* s_rcp, uint32_t* code0, uint32_t* code1) {
+  // straight-line code with short dependency chains (a pairwise max tree, no branch): the
+  // quantiser warps are few, so their throughput is set by latency, not by issue slots
   float2 xh[8];
-  float m = 0.f;
+  float a8[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const float2 xv = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
     xh[k] = ptx::mul2_rn(xv, make_float2(il[2 * k], il[2 * k + 1]));
-    m = fmaxf(m, fmaxf(fabsf(xh[k].x), fabsf(xh[k].y)));
+    a8[k] = fmaxf(fabsf(xh[k].x), fabsf(xh[k].y));
   }
+  const float m = fmaxf(fmaxf(fmaxf(fmaxf(a8[0], a8[1]), fmaxf(a8[2], a8[3])),
+                              fmaxf(fmaxf(a8[4], a8[5]), fmaxf(a8[6], a8[7]))),
+                        0.f);
   int code = int(ptx::cvt_e4m3x2(0.f, __fmul_rn(m, inv_six)) & 0xFF);
   code = code - (m < s_thr[code] ? 1 : 0) + (m >= s_thr[code + 1] ? 1 : 0);
-  *code0 = 0u;
-  *code1 = 0u;
-  if (code != 0) {
-    const float rcp = s_rcp[code];
-    const float2 r2 = make_float2(rcp, rcp);
-    float2 q[8];
+  const float rcp = s_rcp[code];
+  const float2 r2 = make_float2(rcp, rcp);
+  float2 q[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) q[k] = ptx::mul2_rn(xh[k], r2);
-    *code0 = ptx::cvt_e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y);
-    *code1 = ptx::cvt_e2m1x8(q[4].x, q[4].y, q[5].x, q[5].y, q[6].x, q[6].y, q[7].x, q[7].y);
-  }
+  for (int k = 0; k < 8; ++k) q[k] = ptx::mul2_rn(xh[k], r2);
+  const uint32_t c0 = ptx::cvt_e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y);
+  const uint32_t c1 = ptx::cvt_e2m1x8(q[4].x, q[4].y, q[5].x, q[5].y, q[6].x, q[6].y, q[7].x, q[7].y);
+  // a zero scale gives zero codes (x * 0 may be -0, whose E2M1 code is not 0)
+  *code0 = code != 0 ? c0 : 0u;
+  *code1 = code != 0 ? c1 : 0u;
   return uint32_t(code);
 }
 
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float4* p = reinterpret_cast<const float4*>(st + C::X_BYTES + C::L_BYTES) + 4 * t;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float4 v = p[k];
+          const float4 v = p[k ^ (t >> 1)];   // bank-spread layout of the 1/lambda part
           il[4 * k] = v.x; il[4 * k + 1] = v.y; il[4 * k + 2] = v.z; il[4 * k + 3] = v.w;
         }
       }
@@ -280,19 +284,25 @@ __global__ void __launch_bounds__(kThreads, 2)
 
       const int64_t col = int64_t(c) * 64 + 16 * t;
 #pragma unroll
+      // both blocks first (independent chains), then the shuffles, then the stores
+      uint32_t s8[2], code0[2], code1[2], word[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) s8[h] = quant_block(w[h], il, a.inv_six, s_thr, s_rcp, &code0[h], &code1[h]);
+      // the quad's four scale bytes of a row form one 32-bit word of the tiled layout
+#pragma unroll
+      for (int h = 0; h < 2; ++h) word[h] = s8[h] << (8 * t);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) word[h] |= __shfl_xor_sync(kFull, word[h], 1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) word[h] |= __shfl_xor_sync(kFull, word[h], 2);
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t code0, code1;
-        const uint32_t s8 = quant_block(w[h], il, a.inv_six, s_thr, s_rcp, &code0, &code1);
         const int64_t row = row0 + 16 * warp + g + 8 * h;
         if (row < M) {
           uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + col / 2);
-          *dst = make_uint2(code0, code1);
+          *dst = make_uint2(code0[h], code1[h]);
         }
-        // the quad's four scale bytes of this row form one 32-bit word of the tiled layout
-        uint32_t word = s8 << (8 * t);
-        word |= __shfl_xor_sync(kFull, word, 1);
-        word |= __shfl_xor_sync(kFull, word, 2);
-        if (t == h) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word;
+        if (t == h) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word[h];
       }
     }
     // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM
@@ -397,29 +407,51 @@ __global__ void __launch_bounds__(kThreads, 2)
 // K, so the down-projection needs no split and no cross-CTA reduction.  A stage is CH
 // consecutive 64-column chunks (CH x 128 contiguous bytes of every row, so DRAM pages are
 // read in long runs): CH 32 x 64 X tiles (TMA) and the chunks' L1 slices and 1/lambda parts
-// (bulk copies).  The down-projection uses tcgen05.mma with M = 128: rows 32..127 of the A
-// operand run into the following shared memory and only produce TMEM lanes 32..127, which
-// nothing reads (the ring is followed by a pad so those reads stay inside the CTA's shared
-// memory).
+// (bulk copies).
+//
+// Down-projection for r <= 64 (four chunks a stage): the stage's four 32-row X tiles lie back
+// to back, so together they are one 128-row A operand, and the four L1 slices are one
+// (4 r)-row B operand.  One tcgen05.mma with M = 128, N = 4 r per 16-wide k-step multiplies
+// them; block (q, q) of the product (TMEM lanes 32 q .. 32 q + 31, columns q r .. q r + r - 1)
+// is chunk q's contribution to T, the off-diagonal blocks are never read, and T is the sum of
+// the four diagonal blocks at the end.  Against one M = 128, N = r product per chunk (whose
+// rows 32..127 would be wasted) this reads 2.5x fewer operand bytes from shared memory and
+// issues 4x fewer instructions.  For r > 64 each chunk is its own M = 128, N = r product; its A
+// rows 32..127 run into the following shared memory and only produce TMEM lanes 32..127,
+// which nothing reads (a pad after the ring keeps those reads inside the CTA's shared memory).
+//
+// The quantiser warps, not the stream, set the pace of this kernel: a warp's blocks are short
+// dependency chains, so there are as many warps as the register budget allows (16 with four
+// chunks a stage, one 8-row x 64-column piece each).
 constexpr int kTallRows = 32;
 
 template <int R>
 struct TallCfg {
-  static constexpr int CH = R <= 64 ? 4 : 2;                    // chunks per stage
+  static constexpr int CH = R <= 96 ? 4 : 2;                    // chunks per stage
+  static constexpr int QW = 4 * CH;                            // quantiser warps: 8 rows of a chunk each
+  static constexpr int PRODUCER = QW, MMA = QW + 1, THREADS = 32 * (QW + 2);
   static constexpr int X_TILE = kTallRows * 128;               // 32 rows x 64 bf16
   static constexpr int X_BYTES = CH * X_TILE;
   static constexpr int L_BYTES = R * 128;
   static constexpr int LI_BYTES = CH * (L_BYTES + 256);
   static constexpr int STAGE_BYTES = ((X_BYTES + LI_BYTES + 1023) / 1024) * 1024;
   static constexpr int STAGES = (204 * 1024) / STAGE_BYTES > 8 ? 8 : (204 * 1024) / STAGE_BYTES;
-  static constexpr int SPAN = (CH - 1) * X_TILE + 128 * 128;    // farthest A byte read: last tile + 128 rows
+  static constexpr bool STACK = R > 0 && R <= 64;              // one M = 128 product over the four chunks
+  static constexpr int N_MMA = STACK ? CH * R : R;
+  static constexpr int SPAN = STACK ? X_BYTES : (CH - 1) * X_TILE + 128 * 128;   // farthest A byte read
   static constexpr int PAD = SPAN > STAGE_BYTES ? SPAN - STAGE_BYTES : 0;
   static constexpr int SMEM = STAGES * STAGE_BYTES + PAD + 1024;
-  static constexpr int WPC = kQWarps / CH;                     // quantiser warps per chunk
+  static constexpr int WPC = QW / CH;                          // quantiser warps per chunk
   static constexpr int RPT = kTallRows / WPC / 8;              // rows per thread
-  static constexpr uint32_t TMEM_COLS = R <= 32 ? 32 : (R <= 64 ? 64 : 128);
-  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(R >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+  // STACK: every warp quarter q loads 32-column pieces from column q r on
+  static constexpr uint32_t TMEM_COLS = STACK ? (R <= 32 ? 128 : 256) : (R <= 32 ? 32 : (R <= 64 ? 64 : 128));
+  static constexpr uint32_t IDESC =
+      (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N_MMA >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+  static_assert(!STACK || 3 * R + ((R + 31) / 32) * 32 <= int(TMEM_COLS), "TMEM columns");
+  static_assert(!STACK || N_MMA <= 256, "MMA N");
+  static_assert(!STACK || 3 * 32 * R * 4 <= STAGE_BYTES, "reduction buffer fits in one stage");
   static_assert(STAGES >= 3, "stages");
+  static_assert(RPT >= 1 && RPT <= 4, "rows per thread");
 };
 
 // Stage j's L1 slices and 1/lambda parts: [CH slices][CH 1/lambda parts].
@@ -438,9 +470,10 @@ __device__ __forceinline__ void tall_li_loads(unsigned char* dst, const unsigned
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
     k1_tall_kernel(const __grid_constant__ XMap xmap, K1Args a) {
   using C = TallCfg<R>;
+  constexpr int kProducer = C::PRODUCER, kMma = C::MMA, kQWarps = C::QW;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full[C::STAGES], empty[C::STAGES], done;
@@ -526,14 +559,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t xs = ptx::smem_u32(ring + stage * C::STAGE_BYTES);
         const uint32_t ls = xs + C::X_BYTES;
-#pragma unroll
-        for (int cc = 0; cc < C::CH; ++cc)
+        if constexpr (C::STACK) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            ptx::mma_bf16(tmem, ptx::desc_sw128(xs + cc * C::X_TILE + 32 * kk),
-                          ptx::desc_sw128(ls + cc * C::L_BYTES + 32 * kk), C::IDESC, accumulate);
+            ptx::mma_bf16(tmem, ptx::desc_sw128(xs + 32 * kk), ptx::desc_sw128(ls + 32 * kk), C::IDESC, accumulate);
             accumulate = 1;
           }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < C::CH; ++cc)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              ptx::mma_bf16(tmem, ptx::desc_sw128(xs + cc * C::X_TILE + 32 * kk),
+                            ptx::desc_sw128(ls + cc * C::L_BYTES + 32 * kk), C::IDESC, accumulate);
+              accumulate = 1;
+            }
+        }
         ptx::tc_commit(&empty[stage]);
         if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
       }
@@ -565,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* p = reinterpret_cast<const float4*>(st + C::X_BYTES + C::CH * C::L_BYTES + cc * 256) + 4 * t;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float4 v = p[k];
+          const float4 v = p[k ^ (t >> 1)];   // bank-spread layout of the 1/lambda part
           il[4 * k] = v.x; il[4 * k + 1] = v.y; il[4 * k + 2] = v.z; il[4 * k + 3] = v.w;
         }
       }
@@ -575,58 +616,111 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int c = C::CH * j + cc;
       if (c >= nchunks) continue;
+      // all blocks first (independent chains), then the shuffles, then the stores
+      uint32_t s8[C::RPT], code0[C::RPT], code1[C::RPT], word[C::RPT];
+#pragma unroll
+      for (int h = 0; h < C::RPT; ++h) s8[h] = quant_block(w[h], il, a.inv_six, s_thr, s_rcp, &code0[h], &code1[h]);
+#pragma unroll
+      for (int h = 0; h < C::RPT; ++h) word[h] = s8[h] << (8 * t);
+#pragma unroll
+      for (int h = 0; h < C::RPT; ++h) word[h] |= __shfl_xor_sync(kFull, word[h], 1);
+#pragma unroll
+      for (int h = 0; h < C::RPT; ++h) word[h] |= __shfl_xor_sync(kFull, word[h], 2);
 #pragma unroll
       for (int h = 0; h < C::RPT; ++h) {
         const int64_t row = row0 + rbase + g + 8 * h;
-        uint32_t code0, code1;
-        const uint32_t s8 = quant_block(w[h], il, a.inv_six, s_thr, s_rcp, &code0, &code1);
         if (row < M) {
           uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + (int64_t(c) * 64 + 16 * t) / 2);
-          *dst = make_uint2(code0, code1);
+          *dst = make_uint2(code0[h], code1[h]);
         }
-        uint32_t word = s8 << (8 * t);
-        word |= __shfl_xor_sync(kFull, word, 1);
-        word |= __shfl_xor_sync(kFull, word, 2);
-        if (t == h) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word;
+        if (t == h) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word[h];
       }
     }
     // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM
     for (int c = nchunks; c < KG; ++c)
       if (c % C::CH == cc && t < C::RPT)
         *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row0 + rbase + g + 8 * t, c, KG)) = 0u;
+    // rows after the last 32-row tile, up to the end of its 128-row scale tile, belong to no
+    // CTA: the last one writes their scales as zeros
+    if (blockIdx.x == gridDim.x - 1) {
+      const int64_t r_first = row0 + kTallRows, r_end = (row0 / 128) * 128 + 128;
+      const int64_t n = (r_end - r_first) * KG;
+      for (int64_t i = threadIdx.x; i < n; i += 32 * kQWarps)
+        *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(r_first + i / KG, i % KG, KG)) = 0u;
+    }
   }
 
-  // ---- T = (X^ L1) / alpha for the CTA's 32 rows, straight from TMEM lanes 0..31
+  // ---- T = (X^ L1) / alpha for the CTA's 32 rows
   if constexpr (R > 0) {
-    if (warp == 0) {
-      const bool ok = k1_wait(&done, 0, &abort_flag, a.err);
-      ptx::tc_fence_after();
-      const int64_t row = row0 + lane;
-      const int r_pad = a.r_pad;
+    const int64_t row = row0 + lane;
+    uint4* trow = reinterpret_cast<uint4*>(a.T + row * a.r_pad);
+    // 32 columns of T from TMEM (plus the other warps' blocks in `red`), scaled, to bf16
+    auto emit = [&](int cb, const uint32_t* v, const float* red, bool ok) {
 #pragma unroll
-      for (int cb = 0; cb < R; cb += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tmem_slot + cb, v);
-        ptx::tmem_wait_ld();
-        if (row < M) {
-          uint4* dst = reinterpret_cast<uint4*>(a.T + row * r_pad + cb);
+      for (int j = 0; j < 32; j += 8) {
+        if (cb + j < R) {
+          uint32_t o[4];
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            if (cb + j < R) {
-              uint32_t o[4];
+          for (int u = 0; u < 4; ++u) {
+            float y[2];
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                o[u] = ok ? ptx::pack_bf16x2(__uint_as_float(v[j + 2 * u]) * a.inv_alpha,
-                                             __uint_as_float(v[j + 2 * u + 1]) * a.inv_alpha)
-                          : 0u;
-              dst[j / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+            for (int e = 0; e < 2; ++e) {
+              const int col = cb + j + 2 * u + e;
+              y[e] = __uint_as_float(v[j + 2 * u + e]);
+              if (red)
+                y[e] = ((y[e] + red[col * 32 + lane]) + red[(R + col) * 32 + lane]) + red[(2 * R + col) * 32 + lane];
             }
+            o[u] = ok ? ptx::pack_bf16x2(y[0] * a.inv_alpha, y[1] * a.inv_alpha) : 0u;
+          }
+          if (row < M) trow[(cb + j) / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    };
+    if constexpr (C::STACK) {
+      // chunk position q's block lies in TMEM lanes 32 q .. 32 q + 31 from column q r on, so
+      // warp q reads it; warps 1..3 pass theirs to warp 0 through the ring, free once every
+      // quantiser warp is past its last stage (all the ring's copies have landed by then)
+      float* red = reinterpret_cast<float*>(ring);   // [3][r][32 lanes]
+      if (warp < kQWarps) ptx::bar_sync(1, 32 * kQWarps);
+      if (warp < 4) {
+        const bool ok = k1_wait(&done, 0, &abort_flag, a.err);
+        ptx::tc_fence_after();
+        if (warp > 0) {
+#pragma unroll
+          for (int cb = 0; cb < R; cb += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tmem_slot + (uint32_t(32 * warp) << 16) + uint32_t(warp * R + cb), v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (cb + j < R) red[((warp - 1) * R + cb + j) * 32 + lane] = __uint_as_float(v[j]);
+          }
+        }
+        ptx::bar_sync(2, 128);
+        if (warp == 0) {
+#pragma unroll
+          for (int cb = 0; cb < R; cb += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tmem_slot + uint32_t(cb), v);
+            ptx::tmem_wait_ld();
+            emit(cb, v, red, ok);
           }
         }
       }
-      if (row < M)
-        for (int j = R; j < r_pad; j += 8) reinterpret_cast<uint4*>(a.T + row * r_pad + j)[0] = make_uint4(0, 0, 0, 0);
+    } else if (warp == 0) {
+      // one product per chunk: T is TMEM lanes 0..31
+      const bool ok = k1_wait(&done, 0, &abort_flag, a.err);
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int cb = 0; cb < R; cb += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tmem_slot + uint32_t(cb), v);
+        ptx::tmem_wait_ld();
+        emit(cb, v, nullptr, ok);
+      }
     }
+    if (warp == 0 && row < M)
+      for (int j = R; j < a.r_pad; j += 8) trow[j / 8] = make_uint4(0, 0, 0, 0);
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kMma) {
@@ -649,7 +743,7 @@ int launch_tall(const XMap& map, const K1Args& a, const K1Plan& p, cudaStream_t 
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.row_tiles, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -693,7 +787,9 @@ K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count) {
   K1Plan p;
   const int nchunks = int(K / 64);
   // enough 32-row tiles to give every other SM one: whole-K CTAs, no split
-  if (ceil_div(M, kTallRows) * 2 >= sm_count) {
+  // or K short enough that a whole-K CTA beats a split with its cross-CTA reduction (measured:
+  // at K = 3072 the 32-row path wins from M = 64 up, at K = 12288 the split wins below ~2400 rows)
+  if (ceil_div(M, kTallRows) * 2 >= sm_count || nchunks <= 96) {
     p.tall = true;
     p.row_tiles = int(ceil_div(M, kTallRows));
     p.nsplit = 1;

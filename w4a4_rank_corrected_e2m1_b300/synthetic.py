@@ -150,4 +150,6 @@ def parity_cases() -> List[Workload]:
         scaled(QKV, name="qkv_small", M=300, K=512, N=768, rank=32, n_outlier=5),
         scaled(MLP_DOWN, name="down_small", M=130, K=1024, N=512, rank=16),
         scaled(QKV, name="rank64_small", M=257, K=768, N=512, rank=64, n_outlier=8),
+        # long K at small M: the split-K activation kernel, K % 256 != 0
+        scaled(MLP_DOWN, name="down_split", M=300, K=6464, N=512, rank=32),
     ]
