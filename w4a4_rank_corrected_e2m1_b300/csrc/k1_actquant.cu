@@ -283,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
 
       const int64_t col = int64_t(c) * 64 + 16 * t;
-#pragma unroll
       // both blocks first (independent chains), then the shuffles, then the stores
       uint32_t s8[2], code0[2], code1[2], word[2];
 #pragma unroll
@@ -451,7 +450,7 @@ struct TallCfg {
   static_assert(!STACK || N_MMA <= 256, "MMA N");
   static_assert(!STACK || 3 * 32 * R * 4 <= STAGE_BYTES, "reduction buffer fits in one stage");
   static_assert(STAGES >= 3, "stages");
-  static_assert(RPT >= 1 && RPT <= 4, "rows per thread");
+  static_assert(RPT == 1, "one row per thread");
 };
 
 // Stage j's L1 slices and 1/lambda parts: [CH slices][CH 1/lambda parts].
@@ -582,31 +581,35 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ quantiser warps
-    // warp w takes chunk w / WPC of the stage and 32 / WPC of its rows; thread (g, t) takes
-    // the 16-element block at columns 16 t .. 16 t + 15 of rows rbase + g + 8 h, h < RPT
+    // warp w takes chunk w / 4 of the stage and rows 8 (w % 4) .. 8 (w % 4) + 7; thread (g, t)
+    // takes the 16-element block at columns 16 t .. 16 t + 15 of row 8 (w % 4) + g.  Its
+    // addresses are computed once and advance by CH chunks a stage.
     const int cc = warp / C::WPC;
-    const int rbase = (warp % C::WPC) * (kTallRows / C::WPC);
+    const int r = (warp % C::WPC) * 8 + g;                      // r % 8 == g: the swizzle row
+    const int64_t row = row0 + r;
+    const bool live = row < M;
+    unsigned char* code_p = a.x_codes + row * (K / 2) + cc * 32 + 8 * t;
+    unsigned char* scale_p = a.x_scales + scale_word_offset(row, cc, KG);
+    const int xoff = cc * C::X_TILE + r * 128;
+    const int u0off = xoff + (((2 * t) ^ g) << 4), u1off = xoff + (((2 * t + 1) ^ g) << 4);
+    const int iloff = C::X_BYTES + C::CH * C::L_BYTES + cc * 256 + 64 * t;
+    const int kx = t >> 1;                                      // bank-spread layout of 1/lambda
     int stage = 0;
     uint32_t phase = 0;
-    for (int j = 0; j < nsteps; ++j) {
+    for (int j = 0; j < nsteps; ++j, code_p += C::CH * 32, scale_p += C::CH * 512) {
       if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
       const unsigned char* st = ring + stage * C::STAGE_BYTES;
-      uint32_t w[C::RPT][8];
+      uint32_t w[8];
       float il[16];
-#pragma unroll
-      for (int h = 0; h < C::RPT; ++h) {
-        const int r = rbase + g + 8 * h;
-        const unsigned char* rowp = st + cc * C::X_TILE + r * 128;
-        const uint4 u0 = *reinterpret_cast<const uint4*>(rowp + (((2 * t) ^ g) << 4));
-        const uint4 u1 = *reinterpret_cast<const uint4*>(rowp + (((2 * t + 1) ^ g) << 4));
-        w[h][0] = u0.x; w[h][1] = u0.y; w[h][2] = u0.z; w[h][3] = u0.w;
-        w[h][4] = u1.x; w[h][5] = u1.y; w[h][6] = u1.z; w[h][7] = u1.w;
-      }
       {
-        const float4* p = reinterpret_cast<const float4*>(st + C::X_BYTES + C::CH * C::L_BYTES + cc * 256) + 4 * t;
+        const uint4 u0 = *reinterpret_cast<const uint4*>(st + u0off);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(st + u1off);
+        w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
+        w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+        const float4* p = reinterpret_cast<const float4*>(st + iloff);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float4 v = p[k ^ (t >> 1)];   // bank-spread layout of the 1/lambda part
+          const float4 v = p[k ^ kx];
           il[4 * k] = v.x; il[4 * k + 1] = v.y; il[4 * k + 2] = v.z; il[4 * k + 3] = v.w;
         }
       }
@@ -614,32 +617,19 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       if (lane == 0) ptx::mbar_arrive(&empty[stage]);
       if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
 
-      const int c = C::CH * j + cc;
-      if (c >= nchunks) continue;
-      // all blocks first (independent chains), then the shuffles, then the stores
-      uint32_t s8[C::RPT], code0[C::RPT], code1[C::RPT], word[C::RPT];
-#pragma unroll
-      for (int h = 0; h < C::RPT; ++h) s8[h] = quant_block(w[h], il, a.inv_six, s_thr, s_rcp, &code0[h], &code1[h]);
-#pragma unroll
-      for (int h = 0; h < C::RPT; ++h) word[h] = s8[h] << (8 * t);
-#pragma unroll
-      for (int h = 0; h < C::RPT; ++h) word[h] |= __shfl_xor_sync(kFull, word[h], 1);
-#pragma unroll
-      for (int h = 0; h < C::RPT; ++h) word[h] |= __shfl_xor_sync(kFull, word[h], 2);
-#pragma unroll
-      for (int h = 0; h < C::RPT; ++h) {
-        const int64_t row = row0 + rbase + g + 8 * h;
-        if (row < M) {
-          uint2* dst = reinterpret_cast<uint2*>(a.x_codes + row * (K / 2) + (int64_t(c) * 64 + 16 * t) / 2);
-          *dst = make_uint2(code0[h], code1[h]);
-        }
-        if (t == h) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = word[h];
-      }
+      if (C::CH * j + cc >= nchunks) continue;
+      uint32_t code0, code1;
+      const uint32_t s8 = quant_block(w, il, a.inv_six, s_thr, s_rcp, &code0, &code1);
+      // the quad's four scale bytes of this row form one 32-bit word of the tiled layout
+      uint32_t word = s8 << (8 * t);
+      word |= __shfl_xor_sync(kFull, word, 1);
+      word |= __shfl_xor_sync(kFull, word, 2);
+      if (live) *reinterpret_cast<uint2*>(code_p) = make_uint2(code0, code1);
+      if (t == 0) *reinterpret_cast<uint32_t*>(scale_p) = word;
     }
     // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM
     for (int c = nchunks; c < KG; ++c)
-      if (c % C::CH == cc && t < C::RPT)
-        *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row0 + rbase + g + 8 * t, c, KG)) = 0u;
+      if (c % C::CH == cc && t == 0) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = 0u;
     // rows after the last 32-row tile, up to the end of its 128-row scale tile, belong to no
     // CTA: the last one writes their scales as zeros
     if (blockIdx.x == gridDim.x - 1) {
