@@ -39,8 +39,8 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on 
 # sources at capture time: a kernel edited since then reports null traffic.
 NCU_TRAFFIC = {
     ("flux_mlp_up", "k1_actquant"): ("64bbebecfbff2fe4", 28.560640e6 + 2.048e3),
-    ("flux_mlp_up", "k2_fp4gemm"): ("da0881e7e67757fd", 33.013248e6 + 64.824320e6),
-    ("flux_mod", "awq_gemv"): ("b38f04e463acbbf2", 35.471872e6 + 0.0),
+    ("flux_mlp_up", "k2_fp4gemm"): ("ca7ff576c5ebc5a0", 33.06e6 + 63.16e6),
+    ("flux_mod", "awq_gemv"): ("91fc375554c326da", 35.47e6 + 0.0),
 }
 KERNEL_SOURCES = {
     "k1_actquant": ["k1_actquant.cu", "ptx.cuh", "svdq_internal.h"],
