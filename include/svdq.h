@@ -168,10 +168,12 @@ int64_t svdq_scales_bytes(int64_t M, int64_t K);
  * needs clearing by the caller).
  * svdq_workspace_size gives the bytes needed for M rows; svdq_reserve makes the
  * handle allocate (cudaMalloc) and own one for M <= M_max; svdq_set_workspace
- * lends caller memory instead (256-byte aligned, NULL to drop it).  With
- * host_staging != 0 the size also covers the device copies of X and Y used by
- * svdq_linear_forward_host.  Concurrent calls on one handle share the
- * workspace and must be ordered on one stream.
+ * lends caller memory instead (256-byte aligned, NULL to drop it).
+ * host_staging is the number of device staging slots for host X and Y: 0 none,
+ * 1 for svdq_linear_forward_host, 2 (or more, taken as 2) also for
+ * svdq_linear_forward_host_batch; each slot adds M*K*2 + M*N*2 bytes.
+ * Concurrent calls on one handle share the workspace and must be ordered on one
+ * stream.
  */
 svdq_status_t svdq_workspace_size(svdq_handle_t h, int64_t M, int32_t host_staging, size_t* bytes);
 svdq_status_t svdq_reserve(svdq_handle_t h, int64_t M_max, int32_t host_staging);
@@ -218,6 +220,24 @@ svdq_status_t svdq_linear_forward_host(svdq_handle_t h, const uint16_t* X_host, 
                                        int64_t M, void* stream);
 
 /*
+ * svdq_linear_forward_host_batch -- B layer calls on HOST buffers, pipelined: step b reads
+ * X_host[b] (M x K bf16) and writes Y_host[b] (M x N bf16), b < B.  The kernels run on `stream`;
+ * the uploads and downloads run on two copy streams the handle creates on first use.  Steps
+ * alternate between two device staging slots, so step b+1's upload and step b-1's download
+ * overlap step b's kernels and each other.  Returns after every Y_host[b] holds its result.
+ *   X_host, Y_host: arrays of B host pointers (caller-owned; pinned memory lets the copies run
+ *   asynchronously, pageable memory works but serialises them).  Y_host[b] must not overlap any
+ *   X_host[c] or another Y_host[c].
+ *   Work already queued on `stream` completes before the first upload starts.
+ *   Errors: SVDQ_ERR_INVALID_ARG (null handle or pointers, negative M or B),
+ *   SVDQ_ERR_WORKSPACE (no workspace with two staging slots for M), SVDQ_ERR_CUDA.  B == 0
+ *   or M == 0 does nothing.
+ */
+svdq_status_t svdq_linear_forward_host_batch(svdq_handle_t h, const uint16_t* const* X_host,
+                                             uint16_t* const* Y_host, int32_t B, int64_t M,
+                                             void* stream);
+
+/*
  * svdq_linear_forward_noalloc -- the same layer as svdq_linear_forward for callers that must
  * not allocate device memory when they run it: code inside a framework's memory pool or budget,
  * code recorded into a CUDA graph, latency-critical loops that cannot take cudaMalloc's implicit
@@ -251,8 +271,8 @@ const char* svdq_last_error(void);
  * AWQ-style W4A16 linear layer (the modulation / adaptive-normalisation layers)
  *
  * The pages keep 16-bit activations and quantise only the weights to four bits, AWQ style,
- * for the layers that are more sensitive to precision (aiflownews article on Nunchaku, "How
- * Nunchaku four bit quantization actually works").  Readings (the pages give none):
+ * for the layers where 4-bit activations cost too much accuracy (aiflownews article on
+ * Nunchaku, "How Nunchaku four bit quantization actually works").  Readings (the pages give none):
  *   - weights W diag(s) in groups of 64 consecutive input channels of an output row:
  *     asymmetric 4-bit codes q in [0, 15], float32 scale sc and zero point z in [0, 15]:
  *       sc = fl32(max(w_max - w_min, 1e-5) / 15), z = clamp(rint(-w_min / sc), 0, 15),

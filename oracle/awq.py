@@ -1,8 +1,8 @@
 """AWQ-style W4A16 linear layer, restated on the CPU (test infrastructure only).
 
-The pages say that for the adaptive-normalisation and modulation layers, which are more
-sensitive to precision than the transformer blocks, Nunchaku keeps 16-bit activations and
-quantises only the weights to four bits in an AWQ style (aiflownews article on Nunchaku,
+Per the pages, Nunchaku treats the adaptive-normalisation and modulation layers differently
+from the transformer blocks, because 4-bit activations hurt them more: it keeps their
+activations in 16 bits and quantises only their weights to four bits, AWQ style (aiflownews article on Nunchaku,
 "How Nunchaku four bit quantization actually works").  They give no group size, scale
 format or search rule; the readings below are the plainest ones (each also listed in the
 design notes):

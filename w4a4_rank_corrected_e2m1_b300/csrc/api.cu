@@ -104,7 +104,7 @@ struct svdq_layer {
   uint8_t* d_R_codes = nullptr;
   uint8_t* d_R_scales = nullptr;   // tiled, rows padded to 256
   uint16_t* d_L2t = nullptr;       // N x r_pad
-  unsigned char* d_LI = nullptr;   // per chunk: folded + permuted L1 slice, then 1/lambda slice
+  unsigned char* d_LI = nullptr;   // groups of four chunks: folded + permuted L1 slices, then 1/lambda
   float* d_inv_lambda = nullptr;
   float* d_qtab = nullptr;         // activation quantiser tables (thresholds, reciprocals)
   uint16_t* d_bias = nullptr;
@@ -121,17 +121,24 @@ struct svdq_layer {
   size_t ws_bytes = 0;
   bool ws_owned = false;
   int64_t ws_M = 0;
-  bool ws_staging = false;
+  int ws_staging = 0;              // device staging slots for host X / Y (0, 1 or 2)
+  // pipelined host calls (svdq_linear_forward_host_batch): copy streams and slot events,
+  // created on first use
+  cudaStream_t pipe_in = nullptr, pipe_out = nullptr;
+  cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr}, ev_out[2] = {nullptr, nullptr};
   float inv_six = 1.f / 6.f, inv_alpha = 1.f;
 };
 
 namespace {
 
 struct WsLayout {
-  size_t codes, scales, T, partial, arrivals, Xs, Ys, total;
+  size_t codes, scales, T, partial, arrivals, Xs[2], Ys[2], total;
 };
 
-WsLayout ws_layout(const svdq_layer* h, int64_t M, bool staging) {
+// host_staging argument -> number of staging slots
+int staging_slots(int32_t host_staging) { return host_staging <= 0 ? 0 : (host_staging >= 2 ? 2 : 1); }
+
+WsLayout ws_layout(const svdq_layer* h, int64_t M, int staging) {
   WsLayout w{};
   const int64_t K = h->host.K, N = h->host.N, r = h->rank_k();
   size_t off = 0;
@@ -140,8 +147,10 @@ WsLayout ws_layout(const svdq_layer* h, int64_t M, bool staging) {
   w.T = off; off += align256(size_t(M) * h->r_pad * 2);
   w.partial = off; off += align256(k1_partial_bytes(M, int(r)));
   w.arrivals = off; off += align256(r ? k1_arrival_bytes(M) : 0);
-  w.Xs = off; off += staging ? align256(size_t(M) * K * 2) : 0;
-  w.Ys = off; off += staging ? align256(size_t(M) * N * 2) : 0;
+  for (int i = 0; i < 2; ++i) {
+    w.Xs[i] = off; off += i < staging ? align256(size_t(M) * K * 2) : 0;
+    w.Ys[i] = off; off += i < staging ? align256(size_t(M) * N * 2) : 0;
+  }
   w.total = off;
   return w;
 }
@@ -173,6 +182,13 @@ void free_layer(svdq_layer* h) {
   cudaFree(h->d_bias);
   cudaFree(h->d_err);
   if (h->ws_owned) cudaFree(h->ws);
+  if (h->pipe_in) cudaStreamDestroy(h->pipe_in);
+  if (h->pipe_out) cudaStreamDestroy(h->pipe_out);
+  for (int i = 0; i < 2; ++i) {
+    if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+    if (h->ev_comp[i]) cudaEventDestroy(h->ev_comp[i]);
+    if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
+  }
 }
 
 // Device layouts of the low-rank branch for the handle's kernel rank (SVD rank plus any LoRA
@@ -180,7 +196,7 @@ void free_layer(svdq_layer* h) {
 //   LI   per group of four 64-column chunks: the chunks' slices of L1' (rank_k rows of 64
 //        K-values, bf16, K-major, 128-byte rows with the 128-byte swizzle the tensor cores
 //        read: 16-byte unit u of row j stored at unit u ^ (j % 8)), then the chunks' 64 values
-//        of 1/lambda each (fp32).
+//        of 1/lambda each (fp32, in the bank-spread order described where they are written).
 //        L1' = diag(1/lambda) L1 for the SVD columns (kernel 1 multiplies raw X by it, which
 //        is X^ L1), and bf16(scale * A) for the LoRA columns (X A needs no smoothing)
 //   L2t  N x r_pad bf16: L2 transposed, then B transposed, zero padding
@@ -246,14 +262,14 @@ svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
   return SVDQ_OK;
 }
 
-svdq_status_t attach_workspace(svdq_layer* h, void* ptr, size_t bytes, int64_t M_max, bool staging, bool owned,
+svdq_status_t attach_workspace(svdq_layer* h, void* ptr, size_t bytes, int64_t M_max, int staging, bool owned,
                                cudaStream_t stream) {
   if (h->ws_owned && h->ws) cudaFree(h->ws);
   h->ws = static_cast<unsigned char*>(ptr);
   h->ws_bytes = bytes;
   h->ws_owned = owned;
   h->ws_M = ptr ? M_max : 0;
-  h->ws_staging = ptr ? staging : false;
+  h->ws_staging = ptr ? staging : 0;
   (void)stream;
   return SVDQ_OK;
 }
@@ -496,7 +512,7 @@ svdq_status_t svdq_export(svdq_handle_t h, svdq_packed_host_t* out) {
 
 svdq_status_t svdq_workspace_size(svdq_handle_t h, int64_t M, int32_t host_staging, size_t* bytes) {
   if (!h || !bytes || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null argument or negative M");
-  *bytes = ws_layout(h, M, host_staging != 0).total;
+  *bytes = ws_layout(h, M, staging_slots(host_staging)).total;
   return SVDQ_OK;
 }
 
@@ -535,28 +551,28 @@ svdq_status_t svdq_attach_lora(svdq_handle_t h, const uint16_t* A_bf16, const ui
     h->r_lora = old_rl;
     return st;
   }
-  if (h->ws && h->ws_owned && h->ws_bytes < need) return svdq_reserve(h, h->ws_M, h->ws_staging ? 1 : 0);
+  if (h->ws && h->ws_owned && h->ws_bytes < need) return svdq_reserve(h, h->ws_M, h->ws_staging);
   return SVDQ_OK;
 }
 
 svdq_status_t svdq_reserve(svdq_handle_t h, int64_t M_max, int32_t host_staging) {
   if (!h || M_max < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M_max");
   DeviceGuard guard(h->device);
-  const size_t bytes = ws_layout(h, M_max, host_staging != 0).total;
+  const size_t bytes = ws_layout(h, M_max, staging_slots(host_staging)).total;
   cudaError_t e;
   void* p = dalloc(bytes, &e);
   if (e != cudaSuccess) return fail(SVDQ_ERR_OOM, "workspace allocation failed");
-  return attach_workspace(h, p, bytes, M_max, host_staging != 0, true, nullptr);
+  return attach_workspace(h, p, bytes, M_max, staging_slots(host_staging), true, nullptr);
 }
 
 svdq_status_t svdq_set_workspace(svdq_handle_t h, void* dev_ptr, size_t bytes, int64_t M_max, int32_t host_staging) {
   if (!h || M_max < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle or negative M_max");
   DeviceGuard guard(h->device);
-  if (dev_ptr == nullptr) return attach_workspace(h, nullptr, 0, 0, false, false, nullptr);
+  if (dev_ptr == nullptr) return attach_workspace(h, nullptr, 0, 0, 0, false, nullptr);
   if (reinterpret_cast<uintptr_t>(dev_ptr) & 255u) return fail(SVDQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  if (bytes < ws_layout(h, M_max, host_staging != 0).total)
+  if (bytes < ws_layout(h, M_max, staging_slots(host_staging)).total)
     return fail(SVDQ_ERR_WORKSPACE, "workspace smaller than svdq_workspace_size");
-  return attach_workspace(h, dev_ptr, bytes, M_max, host_staging != 0, false, nullptr);
+  return attach_workspace(h, dev_ptr, bytes, M_max, staging_slots(host_staging), false, nullptr);
 }
 
 svdq_status_t svdq_quantize_act(svdq_handle_t h, const void* X, int64_t M, void* x_codes, void* x_scales, void* T,
@@ -609,9 +625,9 @@ svdq_status_t svdq_linear_forward_host(svdq_handle_t h, const uint16_t* X_host, 
     return fail(SVDQ_ERR_WORKSPACE, "needs a workspace reserved with host staging for this M");
   DeviceGuard guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const WsLayout w = ws_layout(h, h->ws_M, true);
-  void* Xd = h->ws + w.Xs;
-  void* Yd = h->ws + w.Ys;
+  const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
+  void* Xd = h->ws + w.Xs[0];
+  void* Yd = h->ws + w.Ys[0];
   cudaError_t e = cudaMemcpyAsync(Xd, X_host, size_t(M) * h->host.K * 2, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "copying X to the device");
   svdq_status_t st = svdq_linear_forward(h, Xd, Yd, M, stream);
@@ -619,6 +635,68 @@ svdq_status_t svdq_linear_forward_host(svdq_handle_t h, const uint16_t* X_host, 
   e = cudaMemcpyAsync(Y_host, Yd, size_t(M) * h->host.N * 2, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "copying Y to the host");
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_linear_forward_host_batch(svdq_handle_t h, const uint16_t* const* X_host, uint16_t* const* Y_host,
+                                             int32_t B, int64_t M, void* stream) {
+  if (!h || M < 0 || B < 0) return fail(SVDQ_ERR_INVALID_ARG, "null handle, negative M or negative batch count");
+  if (M == 0 || B == 0) return SVDQ_OK;
+  if (!X_host || !Y_host) return fail(SVDQ_ERR_INVALID_ARG, "null buffer list");
+  for (int32_t b = 0; b < B; ++b)
+    if (!X_host[b] || !Y_host[b]) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!h->ws || h->ws_staging < 2 || h->ws_M < M)
+    return fail(SVDQ_ERR_WORKSPACE, "needs a workspace reserved with two host staging slots for this M");
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaSuccess;
+  if (!h->pipe_in) {
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->pipe_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->pipe_out, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_comp[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "creating the copy streams and events");
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
+  const size_t xb = size_t(M) * h->host.K * 2, yb = size_t(M) * h->host.N * 2;
+  // everything already queued on the caller's stream comes first
+  e = cudaEventRecord(h->ev_comp[0], s);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_comp[1], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->pipe_in, h->ev_comp[0], 0);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_out[0], s);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_out[1], s);
+  for (int32_t b = 0; b < B && e == cudaSuccess; ++b) {
+    const int k = b & 1;
+    void* Xd = h->ws + w.Xs[k];
+    void* Yd = h->ws + w.Ys[k];
+    // upload of step b once step b - 2's kernels no longer read the slot's X
+    e = cudaStreamWaitEvent(h->pipe_in, h->ev_comp[k], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(Xd, X_host[b], xb, cudaMemcpyHostToDevice, h->pipe_in);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_in[k], h->pipe_in);
+    // kernels of step b once its X is in and step b - 2's Y has left the slot
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_in[k], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_out[k], 0);
+    if (e != cudaSuccess) break;
+    svdq_status_t st = svdq_linear_forward(h, Xd, Yd, M, stream);
+    if (st != SVDQ_OK) {
+      cudaStreamSynchronize(h->pipe_in);
+      cudaStreamSynchronize(h->pipe_out);
+      return st;
+    }
+    e = cudaEventRecord(h->ev_comp[k], s);
+    // download of step b
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->pipe_out, h->ev_comp[k], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(Y_host[b], Yd, yb, cudaMemcpyDeviceToHost, h->pipe_out);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_out[k], h->pipe_out);
+  }
+  const cudaError_t e_in = cudaStreamSynchronize(h->pipe_in);
+  const cudaError_t e_out = cudaStreamSynchronize(h->pipe_out);
+  const cudaError_t e_s = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = e_in != cudaSuccess ? e_in : (e_out != cudaSuccess ? e_out : e_s);
+  if (e != cudaSuccess) return cuda_fail(e, "pipelined host forward");
   return SVDQ_OK;
 }
 
@@ -679,7 +757,7 @@ extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void
   if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
   if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
   if (X == Y) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not alias");
-  const WsLayout w = ws_layout(h, M, false);
+  const WsLayout w = ws_layout(h, M, 0);
   if (w.total > kStaticScratchBytes)
     return fail(SVDQ_ERR_WORKSPACE, "M = " + std::to_string(M) + " needs " + std::to_string(w.total) +
                                         " bytes of scratch; the static scratch holds " +

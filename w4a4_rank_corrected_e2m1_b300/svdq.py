@@ -80,6 +80,7 @@ _SIGS = {
     "svdq_gemm_quantized": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp]),
     "svdq_linear_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_linear_forward_host": (_i32, [_vp, _vp, _vp, _i64, _vp]),
+    "svdq_linear_forward_host_batch": (_i32, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _vp]),
     "svdq_check_error": (_i32, [_vp]),
     "svdq_attach_lora": (_i32, [_vp, _vp, _vp, _i64, ctypes.c_float, _vp]),
     "svdq_awq_pack_host": (_i32, [ctypes.POINTER(AwqParams), ctypes.POINTER(AwqHost)]),
@@ -238,15 +239,17 @@ class Layer:
         check(LIB.svdq_export(self.h, ctypes.byref(s)), "svdq_export")
         return _finish(o, s, self.rank)
 
-    def workspace_size(self, M: int, host_staging: bool = False) -> int:
+    # host_staging: device staging slots for host X / Y (0, 1, or 2 for forward_host_batch);
+    # True / False mean 1 / 0
+    def workspace_size(self, M: int, host_staging: int = 0) -> int:
         n = ctypes.c_size_t()
         check(LIB.svdq_workspace_size(self.h, M, int(host_staging), ctypes.byref(n)), "svdq_workspace_size")
         return n.value
 
-    def reserve(self, M_max: int, host_staging: bool = False):
+    def reserve(self, M_max: int, host_staging: int = 0):
         check(LIB.svdq_reserve(self.h, M_max, int(host_staging)), "svdq_reserve")
 
-    def set_workspace(self, buf, M_max: int, host_staging: bool = False):
+    def set_workspace(self, buf, M_max: int, host_staging: int = 0):
         nbytes = 0 if buf is None else buf.numel() * buf.element_size()
         check(LIB.svdq_set_workspace(self.h, _ptr(buf), nbytes, M_max, int(host_staging)), "svdq_set_workspace")
 
@@ -264,6 +267,16 @@ class Layer:
     def forward_host(self, X_host, Y_host, M, stream=None):
         check(LIB.svdq_linear_forward_host(self.h, _ptr(X_host), _ptr(Y_host), M, _stream(stream)),
               "svdq_linear_forward_host")
+
+    def forward_host_batch(self, X_hosts, Y_hosts, M, stream=None):
+        """len(X_hosts) pipelined layer calls on host buffers (workspace with host_staging=2)."""
+        if len(X_hosts) != len(Y_hosts):
+            raise ValueError("X_hosts and Y_hosts differ in length")
+        B = len(X_hosts)
+        xs = (_vp * max(B, 1))(*[_ptr(x) for x in X_hosts])
+        ys = (_vp * max(B, 1))(*[_ptr(y) for y in Y_hosts])
+        check(LIB.svdq_linear_forward_host_batch(self.h, xs, ys, B, M, _stream(stream)),
+              "svdq_linear_forward_host_batch")
 
     def check_error(self):
         check(LIB.svdq_check_error(self.h), "svdq_check_error")
