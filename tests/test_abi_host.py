@@ -23,6 +23,19 @@ def test_every_declared_symbol_is_exported():
         assert ctypes.cast(getattr(svdq.LIB, n), ctypes.c_void_p).value
 
 
+def test_binding_declares_every_header_function():
+    """The ctypes layer sets argument and result types for every C-ABI function, so no call
+    falls back to ctypes' int defaults (which would truncate pointers and 64-bit sizes)."""
+    missing = [n for n in svdq.header_functions() if n not in svdq._SIGS]
+    assert not missing, missing
+
+
+def test_batch_host_forward_rejects_null_handle():
+    # argument checks run before any device work, so they are testable without a GPU
+    assert svdq.LIB.svdq_linear_forward_host_batch(None, None, None, 1, 1, None) == svdq.ERR_INVALID_ARG
+    assert svdq.LIB.svdq_linear_forward_host(None, None, None, 1, None) == svdq.ERR_INVALID_ARG
+
+
 def test_status_strings():
     for s in range(8):
         assert svdq.LIB.svdq_status_string(s)

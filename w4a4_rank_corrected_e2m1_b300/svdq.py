@@ -81,6 +81,7 @@ _SIGS = {
     "svdq_linear_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_linear_forward_host": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_linear_forward_host_batch": (_i32, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _vp]),
+    "svdq_linear_forward_noalloc": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_check_error": (_i32, [_vp]),
     "svdq_attach_lora": (_i32, [_vp, _vp, _vp, _i64, ctypes.c_float, _vp]),
     "svdq_awq_pack_host": (_i32, [ctypes.POINTER(AwqParams), ctypes.POINTER(AwqHost)]),
@@ -263,6 +264,11 @@ class Layer:
 
     def forward(self, X, Y, M, stream=None):
         check(LIB.svdq_linear_forward(self.h, _ptr(X), _ptr(Y), M, _stream(stream)), "svdq_linear_forward")
+
+    def forward_noalloc(self, X, Y, M, stream=None):
+        """The forward on the library's static scratch (no workspace, no allocation)."""
+        check(LIB.svdq_linear_forward_noalloc(self.h, _ptr(X), _ptr(Y), M, _stream(stream)),
+              "svdq_linear_forward_noalloc")
 
     def forward_host(self, X_host, Y_host, M, stream=None):
         check(LIB.svdq_linear_forward_host(self.h, _ptr(X_host), _ptr(Y_host), M, _stream(stream)),
