@@ -38,9 +38,9 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on 
 # captures summarised under profiles/, keyed by the workload and by a hash of the kernel's
 # sources at capture time: a kernel edited since then reports null traffic.
 NCU_TRAFFIC = {
-    ("flux_mlp_up", "k1_actquant"): ("6c310e3af71c39b6", 28.56e6 + 256.0),
-    ("flux_mlp_up", "k2_fp4gemm"): ("ca7ff576c5ebc5a0", 33.06e6 + 63.16e6),
-    ("flux_mod", "awq_gemv"): ("91fc375554c326da", 35.47e6 + 0.0),
+    ("flux_mlp_up", "k1_actquant"): ("ec467875c6f22f34", 28.56e6 + 256.0),
+    ("flux_mlp_up", "k2_fp4gemm"): ("fbb14fff96e80e4f", 33.06e6 + 63.16e6),
+    ("flux_mod", "awq_gemv"): ("666902da617b3e67", 35.47e6 + 0.0),
 }
 KERNEL_SOURCES = {
     "k1_actquant": ["k1_actquant.cu", "ptx.cuh", "svdq_internal.h"],
@@ -49,17 +49,27 @@ KERNEL_SOURCES = {
 }
 
 
-def ncu_traffic(workload, kernel):
-    """Captured DRAM bytes per launch, or None if absent or the kernel changed since."""
+def kernel_source_hash(kernel):
+    """Hash of a kernel's sources with comments and whitespace removed: a code change alters it,
+    a comment edit does not."""
     import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "w4a4_rank_corrected_e2m1_b300", "csrc", f)) as fh:
+            txt = fh.read()
+        txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)
+        txt = re.sub(r"//[^\n]*", " ", txt)
+        h.update(" ".join(txt.split()).encode())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    """Captured DRAM bytes per launch, or None if absent or the kernel's code changed since."""
     entry = NCU_TRAFFIC.get((workload, kernel))
     if entry is None:
         return None
-    h = hashlib.sha256()
-    for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "w4a4_rank_corrected_e2m1_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return entry[1] if h.hexdigest()[:16] == entry[0] else None
+    return entry[1] if kernel_source_hash(kernel) == entry[0] else None
 
 
 def parse():

@@ -6,8 +6,12 @@
 // input, which the Nunchaku section of the aiflownews article on Nunchaku in Diffusers gives
 // as the reason to fuse them.
 //
-// Work decomposition.  A CTA owns a tile of 128 rows and every nsplit-th 64-column chunk of K
-// (a K split).  At the end each CTA writes its partial down-projection (float32) to
+// Two kernels do this.  k1_tall_kernel (further down) takes 32 rows and the whole of K per CTA;
+// it runs when M fills the GPU with 32-row tiles or K <= 6144.  k1_kernel, described here, splits
+// K for long K at small M.
+//
+// Work decomposition (k1_kernel).  A CTA owns a tile of 128 rows and every nsplit-th 64-column
+// chunk of K (a K split).  At the end each CTA writes its partial down-projection (float32) to
 // the workspace; the last CTA of the row tile to arrive adds the partials in split order
 // (deterministic whatever the arrival order), scales by 1/alpha and writes T in bfloat16.
 // Arrival is counted in one 64-bit word per row tile holding (launch epoch << 8) | count,
@@ -22,7 +26,7 @@
 // (with 1/lambda folded in, transposed and pre-swizzled at pack time) followed by its 64
 // values of 1/lambda (one bulk copy).
 //
-// Roles (320 threads):
+// Roles of k1_kernel (320 threads):
 //   warps 0..7  quantisers: each takes 16 rows of the tile; thread (g = lane/4, t = lane%4)
 //               takes rows g and g+8 and the 16 bf16 at columns 16t..16t+15 of the chunk:
 //               exactly one NVFP4 block, so the block maximum needs no shuffles and a quad
