@@ -26,7 +26,10 @@ Block quantiser Qz(v, s_g), each step a float32 IEEE operation:
 Pins (tests/test_oracle_nvfp4.py): exhaustive tie midpoints and +-1 ulp, a
 brute-force nearest-grid search, torch.float8_e4m3fn on in-range values, two
 hand-worked blocks in tests/golden/, and the block invariants (reconstruction
-error within half a grid step; the block maximum lands on code 6.0).
+error within half a grid step; the block maximum lands on code 6.0).  The global
+scale is pinned to hand values (0x39C30C31 for amax = 1) and to the correctly
+rounded quotient computed in exact rational arithmetic, including an amax where
+two successive roundings (by 6, then by 448) would differ in the last bit.
 """
 from __future__ import annotations
 

@@ -190,16 +190,6 @@ def lora_delta(X_bits, A_bits, B_bits, scale, rows=None):
     return float(scale) * ((bf16_to_f64(Xb) @ bf16_to_f64(A_bits)) @ bf16_to_f64(B_bits))
 
 
-def forward_cols(X_bits, p, rows, cols):
-    """Sampled outputs Y[rows][:, cols] (same arithmetic as forward, fewer weight rows)."""
-    sub = dict(p)
-    sub["R_codes"] = p["R_codes"][cols]
-    sub["R_scales"] = p["R_scales"][cols]
-    sub["L2"] = p["L2"][:, cols] if p["rank"] else p["L2"]
-    sub["bias"] = p["bias"][cols]
-    return forward(X_bits, sub, rows=rows)
-
-
 # ----------------------------------------------------------------------------- references
 def exact_product(X_bits, W_bits, bias_bits) -> np.ndarray:
     """The unquantised layer X W^T + b on the bf16 inputs, float64."""

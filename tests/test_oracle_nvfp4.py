@@ -124,3 +124,48 @@ def test_block_invariants():
     normal = (scales >> 3) > 0
     assert np.all(mag[normal] == 7)
     assert scales[0, 0] == 0 and np.all(codes[0, :16] == 0)
+
+
+# ------------------------------------------------------------------ global scale
+def _f32_nearest(q):
+    """The float32 nearest to a positive rational q, ties to even, in exact integer
+    arithmetic (normal range): independent of numpy's float32 division."""
+    from fractions import Fraction
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1
+    if Fraction(2) ** (e + 1) <= q:
+        e += 1
+    s = q / Fraction(2) ** (e - 23)                 # in [2^23, 2^24)
+    n, rem = divmod(s.numerator, s.denominator)
+    if 2 * rem > s.denominator or (2 * rem == s.denominator and n % 2):
+        n += 1
+    return n * 2.0 ** (e - 23)
+
+
+def _bits(x):
+    return int(np.float32(x).view(np.uint32))
+
+
+def test_global_scale_hand_values():
+    """s_g = fl32(amax / 2688) with 2688 = 6 * 448 (the largest E2M1 magnitude times the
+    largest E4M3 scale), one rounding; 1.0 for an all-zero tensor."""
+    assert nvfp4.global_scale(2688.0) == np.float32(1.0)
+    assert nvfp4.global_scale(0.0) == np.float32(1.0)
+    # fl32(1 / 2688) written out: 0x39C30C31
+    assert _bits(nvfp4.global_scale(1.0)) == 0x39C30C31
+    assert _bits(nvfp4.global_scale(5376.0)) == _bits(2.0)
+
+
+def test_global_scale_is_one_rounding():
+    """amax = 64.0592041015625 (0x42801E50): one correctly rounded quotient gives 0x3CC33A62,
+    while dividing by 6 and then by 448 (two roundings) gives 0x3CC33A61.  The expected bits
+    come from exact rational arithmetic."""
+    from fractions import Fraction
+    a = np.uint32(0x42801E50).view(np.float32)
+    assert _bits(nvfp4.global_scale(a)) == 0x3CC33A62
+    two = np.float32(np.float32(a / np.float32(6)) / np.float32(448))
+    assert _bits(two) == 0x3CC33A61                  # the slip this pin catches
+    rng = np.random.default_rng(11)
+    for v in rng.uniform(1e-3, 1e4, 2000).astype(np.float32):
+        assert _bits(nvfp4.global_scale(v)) == _bits(_f32_nearest(Fraction(float(v)) / 2688))

@@ -56,6 +56,21 @@ def test_smoothing_identity(tiny):
     assert lam[c] == np.float32(np.sqrt(xm / wm))
 
 
+def test_smoothing_zero_guard_and_hand_values():
+    """lambda_c = sqrt(max|X_c| / max|W_c|); a channel whose activation or weight column is all
+    zero keeps lambda = 1 (inv_lambda = 1).  Hand values: max|X| = 4, max|W| = 1 gives lambda 2,
+    inv 0.5; max|X| = 1, max|W| = 4 gives 0.5, inv 2."""
+    bf = lambda a: sq.f64_to_bf16(np.asarray(a, np.float64))
+    X = bf([[4.0, 0.0, 1.0, 3.0, 0.0],
+            [-2.0, 0.0, -1.0, 1.0, 0.0]])
+    W = bf([[1.0, 5.0, 4.0, 0.0, 0.0],
+            [-0.5, -2.0, 0.25, 0.0, 0.0]])
+    lam, inv = sq.smoothing_factors(X, W)
+    assert lam.dtype == np.float32 and inv.dtype == np.float32
+    assert list(lam) == [2.0, 1.0, 0.5, 1.0, 1.0]
+    assert list(inv) == [0.5, 1.0, 2.0, 1.0, 1.0]
+
+
 def test_eckart_young(tiny):
     w, d = tiny
     lam, _ = sq.smoothing_factors(d["X"], d["W"])
