@@ -5,13 +5,18 @@
 One step = one pass of the whole hot path (kernel 1: smoothing + NVFP4 quantisation +
 down-projection; kernel 2: block-scaled FP4 tensor-core GEMM + up-projection + bias) over
 one batch of synthetic FLUX-shaped activations already resident in HBM.  L2 is flushed
-(256 MiB write) before every timed step, outside the timed events.  Prints one JSON line.
+(a 256 MiB read that leaves clean lines) before every timed step, outside the timed events.
+Prints one JSON line.  At one GPU the line also carries a `sweep` of every timed point of the
+FLUX-shaped scope (QKV, MLP up/down, the output projection over tokens and ranks): kernel-by-
+kernel medians with cold and warm L2, the fractions of the FP4 and HBM rooflines and the
+low-rank branch's overhead.
 
 Under torchrun (N > 1) every rank runs its own replica on its own GPU with its own batch
 (the layer shards over tokens with no exchange): weak scaling, time = max over ranks.
 
 --impl reference times the CPU oracle (the plain numpy restatement of the method) on the
-host cores, on a bounded sample of rows of the same workload, in the same metric.
+host cores over all M rows of the same workload (fewer rows per step only if K steps of the
+whole workload would exceed about three minutes), in the same metric.
 """
 from __future__ import annotations
 
@@ -80,6 +85,7 @@ def parse():
     ap.add_argument("--workload", default="flux_mlp_up", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="time the headline workload only")
     return ap.parse_args()
 
 
@@ -142,16 +148,22 @@ def oracle_sample(w, d, p, budget_s=10.0):
     return workload_flops(w, rows) / dt / 1e12, rows, dt
 
 
-def run_reference(args, w):
+def run_reference(args, w, budget_s=180.0):
+    """The oracle forward on the host cores, every step over the workload's M rows (like the
+    cpu_baseline leg of the GPU arm), unless K + 1 such steps would exceed the budget: then each
+    step takes an equal share of the rows, at least 512."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     d = synthetic.make(w)
     from oracle import svdquant as sq
     p = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"])
-    rows = min(w.M, 128)
-    for _ in range(args.warmup):
-        sq.forward(d["X"][:rows], p)
+    t0 = time.perf_counter()
+    sq.forward(d["X"], p)                                 # warm-up over all rows, also the estimate
+    t_full = time.perf_counter() - t0
+    rows = w.M
+    if t_full * (args.steps + 1) > budget_s:
+        rows = max(min(w.M, 512), int(w.M * budget_s / (t_full * (args.steps + 1))))
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
@@ -160,10 +172,11 @@ def run_reference(args, w):
     tot = sum(times)
     val = workload_flops(w, rows) * args.steps / tot / 1e12
     threads = blas_threads()
-    sample = f"{rows} of {w.M} token rows per step (oracle forward, weights pre-packed)"
+    sample = (f"{rows} of {w.M} token rows per step, {args.steps} steps after one warm-up step over all rows "
+              f"(oracle forward; the layer packed once by the oracle)")
     out = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "steps": args.steps, "warmup": 1, "ms_per_step": 1e3 * tot / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "rank": w.rank},
         "tokens_per_s": rows * args.steps / tot,
@@ -280,6 +293,122 @@ class Clocks:
 
 
 # ------------------------------------------------------------------ GPU arm
+class L2Flush:
+    """Evicts L2 between timed steps by reading (not writing) a 256 MiB buffer that was written
+    once at set-up: L2 is left holding clean lines, so the next kernel's reads evict them for
+    free instead of paying the write-back of dirty lines inside its own timed window."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.buf = torch.ones(64 << 20, dtype=torch.int32, device="cuda")
+        self.acc = torch.empty((), dtype=torch.int64, device="cuda")
+
+    def __call__(self):
+        self.torch.sum(self.buf, dim=0, out=self.acc)
+
+
+def k1_bytes(M, K, rank):
+    """Algorithmic HBM bytes of kernel 1: X read, codes, scales and T written, L1 and 1/lambda."""
+    return M * K * 2 + M * K // 2 + M * K // 16 + M * rank * 2 + K * rank * 2 + K * 4
+
+
+class Point:
+    """One workload on one GPU: the packed layer at its rank and at rank 0, resident inputs and
+    outputs, and the kernel-by-kernel buffers."""
+
+    def __init__(self, torch, svdq, w, device, rank_seed=0, nbuf=1):
+        self.torch, self.w = torch, w
+        d = synthetic.make(w)
+        t0 = time.perf_counter()
+        self.layer = svdq.Layer(d["W"], w.rank, bias=d["bias"], Xcal=d["X"], M_max=w.M, device=device)
+        self.pack_s = time.perf_counter() - t0
+        self.layer0 = svdq.Layer(d["W"], 0, bias=d["bias"], Xcal=d["X"], M_max=w.M, device=device)
+        self.d = d
+        M, K, N = w.M, w.K, w.N
+        self.Xs = [torch.from_numpy(synthetic.make_x(w, M, seed=sd).view(np.int16)).cuda()
+                   for sd in batch_seeds(rank_seed, nbuf)]
+        self.Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        self.codes = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+        self.scales = torch.empty(svdq.scales_bytes(M, K), dtype=torch.uint8, device="cuda")
+        self.T = torch.empty((M, max(self.layer.info.r_pad, 8)), dtype=torch.int16, device="cuda")
+
+    def close(self):
+        self.layer.close()
+        self.layer0.close()
+
+
+def time_events(torch, stream, body, reps, warm, flush, marks):
+    """Run body(i, ev) reps + warm times; ev is a list of `marks` events body records on
+    `stream`.  With `flush`, L2 is flushed before every iteration, outside the events.
+    Returns the per-iteration lists of consecutive event gaps (ms) of the timed iterations."""
+    for i in range(warm):
+        if flush:
+            flush()
+        body(i, None)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(reps)]
+    for i in range(reps):
+        if flush:
+            flush()
+        body(i, evs[i])
+    torch.cuda.synchronize()
+    return [[e[j].elapsed_time(e[j + 1]) for j in range(marks - 1)] for e in evs]
+
+
+def measure_point(torch, pt, stream, reps, warm, flush):
+    """Medians (microseconds) of the forward and of kernel 1 and kernel 2 run one at a time, at
+    the point's rank and at rank 0, with L2 flushed before every run (cold) and without (warm)."""
+    lay, lay0, M, nb = pt.layer, pt.layer0, pt.w.M, len(pt.Xs)
+
+    def fwd(layer):
+        def body(i, ev):
+            if ev:
+                ev[0].record(stream)
+            layer.forward(pt.Xs[i % nb], pt.Y, M, stream)
+            if ev:
+                ev[1].record(stream)
+        return body
+
+    def split(layer):
+        def body(i, ev):
+            if ev:
+                ev[0].record(stream)
+            layer.quantize_act(pt.Xs[i % nb], M, pt.codes, pt.scales, pt.T, stream)
+            if ev:
+                ev[1].record(stream)
+            layer.gemm_quantized(pt.codes, pt.scales, pt.T, pt.Y, M, stream)
+            if ev:
+                ev[2].record(stream)
+        return body
+
+    out = {}
+    for mode, fl in (("cold", flush), ("warm", None)):
+        f = time_events(torch, stream, fwd(lay), reps, warm, fl, 2)
+        k = time_events(torch, stream, split(lay), reps, warm, fl, 3)
+        k0 = time_events(torch, stream, split(lay0), reps, warm, fl, 3)
+        med = lambda rows, j: 1e3 * statistics.median(r[j] for r in rows)
+        out[mode] = {"fwd_us": med(f, 0), "k1_us": med(k, 0), "k2_us": med(k, 1),
+                     "k1_rank0_us": med(k0, 0), "k2_rank0_us": med(k0, 1)}
+    lay.check_error()
+    lay0.check_error()
+    return out
+
+
+def point_summary(w, t, hbm, fp4_peak):
+    """Per-point figures of the scope table's measurement row, from measure_point's times."""
+    c = t["cold"]
+    lowrank = ((c["k1_us"] + c["k2_us"]) - (c["k1_rank0_us"] + c["k2_rank0_us"])) / c["k2_rank0_us"]
+    return {
+        "M": w.M, "K": w.K, "N": w.N, "rank": w.rank,
+        "cold_l2": {k: round(v, 2) for k, v in c.items()},
+        "warm_l2": {k: round(v, 2) for k, v in t["warm"].items()},
+        "tflops": workload_flops(w) / (c["fwd_us"] * 1e-6) / 1e12,
+        "tokens_per_s": w.M / (c["fwd_us"] * 1e-6),
+        "frac_fp4_k2": 2.0 * w.M * w.N * w.K / (c["k2_us"] * 1e-6) / 1e12 / fp4_peak,
+        "frac_hbm_k1": k1_bytes(w.M, w.K, w.rank) / (c["k1_us"] * 1e-6) / 1e9 / hbm,
+        "lowrank_overhead": lowrank,
+    }
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -296,68 +425,41 @@ def run_ours(args, w):
         if world > 1:
             dist.barrier()
 
-    d = synthetic.make(w)
-    M, K, N = w.M, w.K, w.N
-    t_pack = time.perf_counter()
-    layer = svdq.Layer(d["W"], w.rank, bias=d["bias"], Xcal=d["X"], M_max=M, device=local)
-    t_pack = time.perf_counter() - t_pack
-    layer0 = svdq.Layer(d["W"], 0, bias=d["bias"], Xcal=d["X"], M_max=M, device=local)
-    stream = torch.cuda.current_stream()
-
+    hbm, bf16, src = peaks()
+    fp4_peak = bf16 * FP4_OVER_BF16
     # distinct activation batches per step (rank-specific seeds), resident in HBM
-    nbuf = 4
-    Xs = [torch.from_numpy(synthetic.make_x(w, M, seed=sd).view(np.int16)).cuda() for sd in batch_seeds(rank, nbuf)]
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    pt = Point(torch, svdq, w, local, rank_seed=rank, nbuf=4)
+    layer, M, K, N = pt.layer, w.M, w.K, w.N
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(torch)
 
-    def timed_loop(fn, steps, warm):
-        for i in range(warm):
-            fn(i)
-        torch.cuda.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for i in range(steps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            fn(i)
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in ev]
-
+    # ---- the headline: K timed forwards, L2 flushed before each (outside the events)
+    for i in range(args.warmup):
+        flush()
+        layer.forward(pt.Xs[i % 4], pt.Y, M, stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
     clocks = Clocks(torch.cuda.current_device())
-    fwd_ms = timed_loop(lambda i: layer.forward(Xs[i % nbuf], Y, M, stream), args.steps, args.warmup)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        ev[i][0].record(stream)
+        layer.forward(pt.Xs[i % 4], pt.Y, M, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
     clk = clocks.stop()
+    barrier()
+    torch.cuda.synchronize()
+    fwd_ms = [a.elapsed_time(b) for a, b in ev]
     layer.check_error()
 
-    # per-kernel times through the same kernels called one at a time
-    codes = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
-    scales = torch.empty(svdq.scales_bytes(M, K), dtype=torch.uint8, device="cuda")
-    T = torch.empty((M, max(layer.info.r_pad, 8)), dtype=torch.int16, device="cuda")
-    k_ev = []
+    # ---- kernel by kernel, at the layer's rank and at rank 0 (cold and warm L2)
+    reps = max(100, args.steps)
+    t = measure_point(torch, pt, stream, reps, 10, flush)
 
-    def split_step(i):
-        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        e0.record(stream)
-        layer.quantize_act(Xs[i % nbuf], M, codes, scales, T, stream)
-        e1.record(stream)
-        layer.gemm_quantized(codes, scales, T, Y, M, stream)
-        e2.record(stream)
-        k_ev.append((e0, e1, e2))
-
-    timed_loop(split_step, args.steps, args.warmup)
-    k_ev = k_ev[args.warmup:]
-    t_k1 = statistics.median(a.elapsed_time(b) for a, b, _ in k_ev)
-    t_k2 = statistics.median(b.elapsed_time(c) for _, b, c in k_ev)
-    layer.check_error()
-
-    # the same layer with the low-rank branch removed (rank 0): the branch's added time
-    r0_ms = timed_loop(lambda i: layer0.forward(Xs[i % nbuf], Y, M, stream), args.steps, args.warmup)
-
-    # end to end through the pipelined host-buffer entry point: every step uploads its own X
-    # from pinned host memory and downloads its Y; uploads, kernels and downloads of
+    # ---- end to end through the pipelined host-buffer entry point: every step uploads its own
+    # X from pinned host memory and downloads its Y; uploads, kernels and downloads of
     # neighbouring steps overlap (two staging slots); host wall time over the whole batch
     layer.reserve(M, host_staging=2)
     Xh = [torch.from_numpy(synthetic.make_x(w, M, seed=77 + 2 * rank + i).view(np.int16)).pin_memory()
@@ -374,24 +476,37 @@ def run_ours(args, w):
         e2e_t.append((time.perf_counter() - t0) / n_e2e)
     barrier()
 
-    # max over ranks
     ms_step, e2e_med = max_over_ranks([sum(fwd_ms) / len(fwd_ms), statistics.median(e2e_t)], world, "cuda")
 
+    # ---- every other timed point of the scope table (one GPU only: the scaling runs time the
+    # headline alone)
+    sweep = {}
+    if world == 1 and not args.no_sweep:
+        for sw in synthetic.SWEEP:
+            if sw.name == w.name:
+                sweep[sw.name] = point_summary(sw, t, hbm, fp4_peak)
+                continue
+            p2 = Point(torch, svdq, sw, local)
+            sweep[sw.name] = point_summary(sw, measure_point(torch, p2, stream, 100, 10, flush), hbm, fp4_peak)
+            p2.close()
+            del p2
+            torch.cuda.empty_cache()
+
     if rank == 0:
-        hbm, bf16, src = peaks()
-        fp4_peak = bf16 * FP4_OVER_BF16
         flops = workload_flops(w)
         tflops = job_rate(flops, world, ms_step * 1e-3) / 1e12
+        c = t["cold"]
+        t_k1, t_k2 = c["k1_us"] * 1e-3, c["k2_us"] * 1e-3
         k2_fp4_flops = 2.0 * M * N * K
         k2_achieved = k2_fp4_flops / (t_k2 * 1e-3) / 1e12
-        k1_bytes = M * K * 2 + M * K // 2 + M * K // 16 + M * w.rank * 2 + K * w.rank * 2 + K * 4
-        r0_step = sum(r0_ms) / len(r0_ms)
+        kb = k1_bytes(M, K, w.rank)
+        head = point_summary(w, t, hbm, fp4_peak)
         out = {
             "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "nvfp4(e2m1,e4m3)+bf16, f32 accumulate", "data": "synthetic",
             "config": {"workload": w.name, "M": M, "K": K, "N": N, "rank": w.rank, "per_gpu_tokens": M,
-                       "l2": "flushed before every timed step (256 MiB write outside the timed events)",
+                       "l2": "flushed before every timed step (a 256 MiB read, outside the timed events)",
                        "parallelism": f"replicas x{world} (token shards, no collective)"},
             "tokens_per_s": job_rate(M, world, ms_step * 1e-3),
             "kernels_ms": {"k1_actquant": t_k1, "k2_fp4gemm": t_k2},
@@ -400,32 +515,39 @@ def run_ours(args, w):
                          "traffic": ncu_traffic(w.name, "k2_fp4gemm"), "traffic_unit": "bytes per launch (ncu)",
                          "algorithmic_flop": k2_fp4_flops,
                          "peak_source": f"{src} bf16 {bf16} TFLOP/s x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
-            "roofline_k1": {"bound": "hbm", "kernel": "k1_actquant", "achieved": k1_bytes / (t_k1 * 1e-3) / 1e9,
-                            "peak": hbm, "unit": "GB/s", "frac": k1_bytes / (t_k1 * 1e-3) / 1e9 / hbm,
+            "roofline_k1": {"bound": "hbm", "kernel": "k1_actquant", "achieved": kb / (t_k1 * 1e-3) / 1e9,
+                            "peak": hbm, "unit": "GB/s", "frac": kb / (t_k1 * 1e-3) / 1e9 / hbm,
                             "traffic": ncu_traffic(w.name, "k1_actquant"), "traffic_unit": "bytes per launch (ncu)",
-                            "algorithmic_bytes": k1_bytes},
-            "lowrank": {"rank": w.rank, "fwd_ms": ms_step, "fwd_rank0_ms": r0_step,
-                        "added_frac_of_4bit_gemm": (ms_step - r0_step) / t_k2},
+                            "algorithmic_bytes": kb},
+            "lowrank": {"rank": w.rank, "k1_us": c["k1_us"], "k2_us": c["k2_us"],
+                        "k1_rank0_us": c["k1_rank0_us"], "k2_rank0_us": c["k2_rank0_us"],
+                        "overhead_frac_of_plain_4bit_gemm": head["lowrank_overhead"],
+                        "formula": "[t(K1) + t(K2)] - [t(K1, r=0) + t(K2, r=0)], over t(K2, r=0); cold L2, medians"},
             "e2e": {"value": job_rate(flops, world, e2e_med) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
                     "ms_per_step": e2e_med * 1e3, "steps_per_call": n_e2e,
                     "api": "svdq_linear_forward_host_batch (pipelined, two staging slots)"},
             "gpu_launches": 2 * args.steps,
             "clocks": clk,
-            "pack_s": t_pack,
+            "pack_s": pt.pack_s,
         }
+        if sweep:
+            out["sweep"] = sweep
+            out["sweep_note"] = ("per point: medians of 100 CUDA-event timings after 10 warm-ups; cold_l2 = "
+                                 "256 MiB read before every run, warm_l2 = back to back; fwd = the layer call, "
+                                 "k1/k2 = the kernels called one at a time; tflops, tokens_per_s, fractions "
+                                 "and lowrank_overhead from the cold times")
         if not args.no_cpu_baseline:
             exp = layer.export()
             rc = exp["R_codes"]
             exp["R_codes"] = np.stack([rc & 0xF, rc >> 4], axis=-1).reshape(rc.shape[0], -1)
-            v, rows, dt = oracle_sample(w, d, exp)
+            v, rows, dt = oracle_sample(w, pt.d, exp)
             threads = blas_threads()
             out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
                                    "threads": threads, "kind": "oracle",
                                    "sample": f"oracle forward on {rows} of {M} token rows ({dt:.2f} s) with the layer's packed operands"}
         print(json.dumps(out), flush=True)
-    layer.close()
-    layer0.close()
+    pt.close()
     if world > 1:
         dist.destroy_process_group()
 
@@ -457,7 +579,7 @@ def run_awq(args, w):
     stream = torch.cuda.current_stream()
     Xs = [torch.from_numpy(synthetic.make_x(w, w.M, seed=sd).view(np.int16)).cuda() for sd in batch_seeds(rank, 4)]
     Y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     for i in range(args.warmup):
         layer.forward(Xs[i % 4], Y, w.M, stream)
     torch.cuda.synchronize()
@@ -466,7 +588,7 @@ def run_awq(args, w):
     clocks = Clocks(torch.cuda.current_device())
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         layer.forward(Xs[i % 4], Y, w.M, stream)
         ev[i][1].record(stream)
@@ -486,7 +608,7 @@ def run_awq(args, w):
             "vs_baseline": None, "dtype": "u4 weights (group 64, f32 scale, zero point) x bf16 acts; f16 products, f32 sums",
             "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "group": 64,
-                       "l2": "flushed before every timed step (256 MiB write outside the timed events)",
+                       "l2": "flushed before every timed step (a 256 MiB read, outside the timed events)",
                        "parallelism": f"replicas x{world}"},
             "tokens_per_s": job_rate(w.M, world, ms * 1e-3),
             "roofline": {"bound": "hbm", "kernel": "awq_gemv", "achieved": per_gpu, "peak": hbm, "unit": "GB/s",

@@ -204,8 +204,9 @@ svdq_status_t svdq_gemm_quantized(svdq_handle_t h, const void* x_codes, const vo
 
 /*
  * svdq_linear_forward -- the layer: kernel 1 then kernel 2 on `stream`.
- * X: device M x K bf16 (read once).  Y: device M x N bf16 (written once, must
- * not alias X).  Needs a workspace for M (svdq_reserve / svdq_set_workspace).
+ * X: device M x K bf16 (read once).  Y: device M x N bf16 (written once).  Needs a
+ * workspace for M (svdq_reserve / svdq_set_workspace).  X and Y must not overlap each other
+ * or the workspace's kernel scratch: SVDQ_ERR_INVALID_ARG otherwise.
  */
 svdq_status_t svdq_linear_forward(svdq_handle_t h, const void* X_bf16, void* Y_bf16, int64_t M,
                                   void* stream);
@@ -239,16 +240,23 @@ svdq_status_t svdq_linear_forward_host_batch(svdq_handle_t h, const uint16_t* co
 
 /*
  * svdq_linear_forward_noalloc -- the same layer as svdq_linear_forward for callers that must
- * not allocate device memory when they run it: code inside a framework's memory pool or budget,
- * code recorded into a CUDA graph, latency-critical loops that cannot take cudaMalloc's implicit
- * synchronisation.  Instead of the handle's workspace it uses a statically sized scratch array
- * that the library holds on every device it is loaded on (32 MiB per device, kept until the
- * process exits), so the call makes no allocation of any kind.  It is not described by the
- * SVDQuant/Nunchaku pages; it is an interface convenience of this library.
- *   X: device M x K bf16, Y: device M x N bf16 (as svdq_linear_forward).
- *   The first call on a device looks up the scratch array's device address (once per device,
- *   with that device current); make that first call before any stream capture.
- *   Every call shares the one scratch array: calls that overlap on the GPU (different streams,
+ * not allocate device memory when they run it: code inside a framework's memory pool or budget
+ * (a library-owned cudaMalloc would bypass the pool and may not fit), and latency-critical
+ * loops that cannot take cudaMalloc's implicit synchronisation.  Instead of the handle's
+ * workspace it uses a statically sized scratch array that the library holds on every device it
+ * is loaded on (32 MiB per device, kept until the process exits), so the call makes no
+ * allocation of any kind.  The SVDQuant/Nunchaku pages have no counterpart; it is an interface
+ * convenience of this library.
+ *   X: device M x K bf16, Y: device M x N bf16 (as svdq_linear_forward); neither may overlap
+ *   the other or the static scratch (SVDQ_ERR_INVALID_ARG).
+ *   The scratch array's device address is looked up with cudaGetSymbolAddress, with the
+ *   handle's device current, on every call made outside stream capture, so a device reset
+ *   between calls does no harm.  A call on a stream that is capturing uses the address found by
+ *   the last call outside capture on that device, and fails with SVDQ_ERR_INVALID_ARG if there
+ *   was none: make the first call on a device before any stream capture.
+ *   Every call shares the one scratch array, which keeps the last call's contents (nothing in it
+ *   needs clearing: kernel 2 reads only what kernel 1 wrote in the same call, and the split-K
+ *   arrival words carry a per-launch epoch).  Calls that overlap on the GPU (different streams,
  *   or different handles on the same device without ordering) race on it.  Order them on one
  *   stream.
  *   Errors: SVDQ_ERR_WORKSPACE when M needs more scratch than 32 MiB (svdq_workspace_size with

@@ -158,15 +158,9 @@ def alpha(p) -> np.float32:
     return np.float32(np.float32(p["s_gX"]) * np.float32(p["s_gW"]))
 
 
-def forward(X_bits, p, rows=None):
-    """Y = alpha * deq(Q4(X^)) deq(Q4(R))^T + (X^ L1) L2 + b in float64.
-
-    `rows` restricts the evaluation to a subset of token rows (exactly the same
-    per-row computation, used to sample outputs of large problems).
-    """
+def forward(X_bits, p):
+    """Y = alpha * deq(Q4(X^)) deq(Q4(R))^T + (X^ L1) L2 + b in float64."""
     Xb = np.asarray(X_bits)
-    if rows is not None:
-        Xb = Xb[rows]
     cx, sx, xh = quantize_act(Xb, p["inv_lambda"], p["s_gX"])
     Xdq = nvfp4.dequantize_blocks(cx, sx)
     Rdq = nvfp4.dequantize_blocks(p["R_codes"], p["R_scales"])

@@ -70,5 +70,29 @@ def assert_y_close(Y: np.ndarray, ref: np.ndarray, what=""):
     return rel, mx
 
 
+# Per-tile check: each 256 x 256 output tile (the GEMM's pair tile) on its own, so that an error
+# confined to some TMEM lanes, one epilogue warp's rows or one tile cannot hide in the global
+# norm.  A tile's error is the same mix of bf16 output rounding and 4-bit product noise as the
+# whole output's (about 3e-3 relative), so twice the global bound leaves a wide margin.
+Y_TILE_REL_FRO = 1e-2
+
+
+def assert_tiles_close(Y: np.ndarray, ref: np.ndarray, what="", tile=256):
+    M, N = ref.shape
+    worst = (0.0, None)
+    for m0 in range(0, M, tile):
+        for n0 in range(0, N, tile):
+            r = ref[m0:m0 + tile, n0:n0 + tile]
+            nr = np.linalg.norm(r)
+            if nr == 0:
+                assert np.all(Y[m0:m0 + tile, n0:n0 + tile] == 0), f"{what}: tile ({m0}, {n0})"
+                continue
+            e = float(np.linalg.norm(Y[m0:m0 + tile, n0:n0 + tile] - r) / nr)
+            if e > worst[0]:
+                worst = (e, (m0, n0))
+    assert worst[0] <= Y_TILE_REL_FRO, f"{what}: tile {worst[1]} rel_fro={worst[0]:.3e}"
+    return worst
+
+
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     return sq.bf16_to_f64(b)

@@ -335,6 +335,12 @@ svdq_status_t launch_k2(svdq_layer* h, const void* codes, const void* scales, co
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
 }  // namespace
 
 extern "C" {
@@ -603,11 +609,16 @@ svdq_status_t svdq_linear_forward(svdq_handle_t h, const void* X, void* Y, int64
   if (M == 0) return SVDQ_OK;
   if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
   if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
-  if (X == Y) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not alias");
+  const size_t xb = size_t(M) * h->host.K * 2, yb = size_t(M) * h->host.N * 2;
+  if (overlaps(X, xb, Y, yb)) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap");
   if (!h->ws || h->ws_M < M) return fail(SVDQ_ERR_WORKSPACE, "no workspace for this M (svdq_reserve)");
+  const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
+  // the kernels' scratch part of the workspace (the host staging slots after it are X and Y of
+  // the host-buffer entry points)
+  if (overlaps(X, xb, h->ws, w.Xs[0]) || overlaps(Y, yb, h->ws, w.Xs[0]))
+    return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap the workspace");
   DeviceGuard guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
   void* codes = h->ws + w.codes;
   void* scales = h->ws + w.scales;
   void* T = h->rank_k() ? h->ws + w.T : nullptr;
@@ -718,14 +729,13 @@ svdq_status_t svdq_check_error(svdq_handle_t h) {
 // ------------------------------------------------------------------ forward without allocation
 // Some callers cannot allocate device memory at the point where they run a layer: code running
 // under a framework's memory pool or budget (where a library-owned cudaMalloc would bypass the
-// pool and may not fit), code recorded into a CUDA graph (where cudaMalloc is not a capturable
-// operation), or latency-critical loops where cudaMalloc's implicit device synchronisation is not
-// acceptable.  svdq_linear_forward_noalloc serves them: its scratch (quantised activations, T and
-// kernel 1's split-K partial sums and arrival words) lives in one statically sized device array
-// that the library holds on every device it is loaded on, so the call itself allocates nothing.
-// Nothing in it needs clearing between calls: kernel 2 reads only bytes kernel 1 wrote earlier in
-// the same call, and the arrival words carry a per-launch epoch that makes stale contents
-// (another layer's, or an aborted call's) restart the count.
+// pool and may not fit), or latency-critical loops where cudaMalloc's implicit device
+// synchronisation is not acceptable.  svdq_linear_forward_noalloc serves them: its scratch
+// (quantised activations, T and kernel 1's split-K partial sums and arrival words) lives in one
+// statically sized device array that the library holds on every device it is loaded on, so the
+// call itself allocates nothing.  Nothing in it needs clearing between calls: kernel 2 reads
+// only bytes kernel 1 wrote earlier in the same call, and the arrival words carry a per-launch
+// epoch that makes stale contents (another layer's, or an aborted call's) restart the count.
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB per device
@@ -734,15 +744,27 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 std::mutex g_static_mu;
 void* g_static_ptr[64] = {nullptr};
 
-// Device address of g_static_scratch on the current device (looked up once per device).
-svdq_status_t static_scratch(int device, unsigned char** out) {
+// Device address of g_static_scratch on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address comes from cudaGetSymbolAddress with the device
+// current.  Outside stream capture it is looked up on every call (cheap), so an address made
+// stale by a device reset is never used; inside a capture the address cached by the last call
+// outside one is used, since the capture must not be disturbed by a first-time module load.
+svdq_status_t static_scratch(int device, cudaStream_t stream, unsigned char** out) {
   if (device < 0 || device >= 64) return fail(SVDQ_ERR_INVALID_ARG, "device ordinal out of range");
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();                       // not sticky: clear it and take the cached address
+    cap = cudaStreamCaptureStatusActive;
+  }
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[device]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
     g_static_ptr[device] = p;
+  } else if (!g_static_ptr[device]) {
+    return fail(SVDQ_ERR_INVALID_ARG,
+                "the first svdq_linear_forward_noalloc call on a device must come before any stream capture");
   }
   *out = static_cast<unsigned char*>(g_static_ptr[device]);
   return SVDQ_OK;
@@ -756,17 +778,20 @@ extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void
   if (M == 0) return SVDQ_OK;
   if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
   if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
-  if (X == Y) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not alias");
+  const size_t xb = size_t(M) * h->host.K * 2, yb = size_t(M) * h->host.N * 2;
+  if (overlaps(X, xb, Y, yb)) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap");
   const WsLayout w = ws_layout(h, M, 0);
   if (w.total > kStaticScratchBytes)
     return fail(SVDQ_ERR_WORKSPACE, "M = " + std::to_string(M) + " needs " + std::to_string(w.total) +
                                         " bytes of scratch; the static scratch holds " +
                                         std::to_string(kStaticScratchBytes) + " bytes");
   DeviceGuard guard(h->device);
-  unsigned char* ws = nullptr;
-  svdq_status_t st = static_scratch(h->device, &ws);
-  if (st != SVDQ_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* ws = nullptr;
+  svdq_status_t st = static_scratch(h->device, s, &ws);
+  if (st != SVDQ_OK) return st;
+  if (overlaps(X, xb, ws, kStaticScratchBytes) || overlaps(Y, yb, ws, kStaticScratchBytes))
+    return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap the static scratch");
   K1Args a{};
   k1_scratch(&a, ws, w);
   a.X = static_cast<const uint16_t*>(X);
@@ -921,7 +946,8 @@ svdq_status_t svdq_awq_forward(svdq_awq_handle_t h, const void* X, void* Y, int6
   if (M == 0) return SVDQ_OK;
   if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
   if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
-  if (X == Y) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not alias");
+  if (overlaps(X, size_t(M) * h->host.K * 2, Y, size_t(M) * h->host.N * 2))
+    return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap");
   DeviceGuard guard(h->device);
   AwqArgs a{};
   a.X = static_cast<const uint16_t*>(X);

@@ -78,6 +78,9 @@ MOD = _flux("flux_mod", 1, 3072, 6 * 3072, 0)
 MOD_CFG = _flux("flux_mod_cfg", 2, 3072, 6 * 3072, 0)
 AWQ_WORKLOADS = [MOD, MOD_CFG]
 
+# every timed point of the FLUX-shaped scope, the headline (MLP up) first
+SWEEP = [MLP_UP, QKV, MLP_DOWN, *OPROJ_M, *OPROJ_R]
+
 WORKLOADS: Dict[str, Workload] = {w.name: w for w in [TINY, QKV, MLP_UP, MLP_DOWN, *OPROJ_M, *OPROJ_R, *AWQ_WORKLOADS]}
 
 
