@@ -609,9 +609,9 @@ svdq_status_t svdq_linear_forward(svdq_handle_t h, const void* X, void* Y, int64
   if (M == 0) return SVDQ_OK;
   if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
   if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (!h->ws || h->ws_M < M) return fail(SVDQ_ERR_WORKSPACE, "no workspace for this M (svdq_reserve)");
   const size_t xb = size_t(M) * h->host.K * 2, yb = size_t(M) * h->host.N * 2;
   if (overlaps(X, xb, Y, yb)) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap");
-  if (!h->ws || h->ws_M < M) return fail(SVDQ_ERR_WORKSPACE, "no workspace for this M (svdq_reserve)");
   const WsLayout w = ws_layout(h, h->ws_M, h->ws_staging);
   // the kernels' scratch part of the workspace (the host staging slots after it are X and Y of
   // the host-buffer entry points)
@@ -778,13 +778,13 @@ extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void
   if (M == 0) return SVDQ_OK;
   if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
   if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
-  const size_t xb = size_t(M) * h->host.K * 2, yb = size_t(M) * h->host.N * 2;
-  if (overlaps(X, xb, Y, yb)) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap");
   const WsLayout w = ws_layout(h, M, 0);
   if (w.total > kStaticScratchBytes)
     return fail(SVDQ_ERR_WORKSPACE, "M = " + std::to_string(M) + " needs " + std::to_string(w.total) +
                                         " bytes of scratch; the static scratch holds " +
                                         std::to_string(kStaticScratchBytes) + " bytes");
+  const size_t xb = size_t(M) * h->host.K * 2, yb = size_t(M) * h->host.N * 2;
+  if (overlaps(X, xb, Y, yb)) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap");
   DeviceGuard guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* ws = nullptr;
