@@ -289,9 +289,11 @@ const char* svdq_last_error(void);
  *     a_c = mean_m |Xcal_mc|, alpha in {0, 0.05, ..., 0.95} picked by the smallest
  *     calibration output error (all ones without calibration data)
  *   - forward: x' = fl32(x * fl32(1 / s_c)), Y = x' ((q - z) sc)^T + b, bf16 out; the kernel
- *     multiplies in fp16 (x' rounded to fp16) and sums eight products in fp16 before
- *     float32, so |x'| must stay below 546.  Built for the small-M (GEMV-like) modulation shapes: the weights are
- *     streamed from HBM once per 8 rows of X.
+ *     multiplies in fp16 (x' rounded to fp16) and sums four products in fp16 before float32.
+ *     A row of x' whose largest magnitude exceeds 512 is scaled by an exact power of two for
+ *     the fp16 part and its sums scaled back, so no input magnitude overflows the fp16 sums.
+ *     Built for the small-M (GEMV-like) modulation shapes: the weights are streamed from HBM
+ *     once per 8 rows of X.
  * ================================================================================== */
 typedef struct svdq_awq_layer* svdq_awq_handle_t;
 

@@ -85,3 +85,24 @@ def test_awq_errors_and_m_zero():
         layer.forward(X, X, 1)                                   # aliasing
     assert e.value.status == svdq.ERR_INVALID_ARG
     layer.close()
+
+
+@pytest.mark.parametrize("amp", [400.0, 560.0, 3000.0, 60000.0])
+def test_awq_large_activations_do_not_overflow(amp):
+    """Rows of x' far beyond the range where four fp16 products x' (q - z) would overflow
+    (|x'| * 15 * 4 > 65504 from |x'| ~ 1092): the kernel scales such a row by a power of two
+    for its fp16 part.  One row stays small (scale 1), the others peak at `amp`; Y is finite
+    and matches the oracle within the layer's tolerance."""
+    w, d, _ = _case(4, 1024, 520, seed=23)
+    layer = svdq.AwqLayer(d["W"], bias=d["bias"])          # s = 1: x' = x
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((4, 1024))
+    X[1:] *= amp / np.max(np.abs(X[1:]), axis=1, keepdims=True)
+    Xb = synthetic.f64_to_bf16_bits(X)
+    o = layer.export()
+    Y = _run(layer, Xb, 4)
+    assert np.all(np.isfinite(Y))
+    ref = awq.forward(Xb, _oracle_packed(o))
+    for m in range(4):
+        gh.assert_y_close(Y[m:m + 1], ref[m:m + 1], f"awq row {m} amp={amp}")
+    layer.close()

@@ -20,8 +20,11 @@
 //   * two 16-byte words' products (eight per half) are summed in fp16 and added into a float32
 //     total, which the group scale multiplies once per 32 weights;
 //   * the warp reduces its lanes with shuffles and writes bf16(acc + b).
-// fp16 keeps 11 bits of the products (|x'| must stay below 65504 / (8 * 15) for the sums of
-// eight products); longer sums are float32.
+// fp16 keeps 11 bits of the products; longer sums are float32.  A half2 lane sums four products
+// x' (q - z) with |q - z| <= 15, so a row of x' whose largest magnitude exceeds 512 is first
+// scaled by an exact power of two 2^-s (s chosen per row from that magnitude) and its sums
+// multiplied back by 2^s: every fp16 sum then stays below 4 * 512 * 15 = 30720 < 65504, for any
+// input, and rows within 512 (s = 0) are computed exactly as without the scaling.
 // Every wait is bounded (about two seconds; on expiry the error word is set and the block
 // returns).
 #include <cuda_fp16.h>
@@ -90,6 +93,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, i
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ uint64_t full[8], empty[8];
   __shared__ volatile int abort_flag;
+  __shared__ unsigned int row_max_bits[MB];
   const int64_t K = a.K, N = a.N;
   const int nseg = int(K / 32);
   const int64_t KG = K / 64;
@@ -109,6 +113,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, i
       ptx::mbar_init(&full[i], 1);
       ptx::mbar_init(&empty[i], kWarps);
     }
+    for (int m = 0; m < MB; ++m) row_max_bits[m] = 0u;
     abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -143,8 +148,48 @@ __global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, i
     }
   } else {
     // ------------------------------------------------------------ compute warps
-    // x' = fl32(x * fl32(1 / s)) rounded to fp16, in the paired segment order: a thread takes 8
-    // channels (one 16-byte load of X) and writes them as one 16-byte word of a segment
+    // largest |x'| of each row, then the row's power-of-two scaling 2^-shift[m] (see the header)
+    {
+      float mx[MB];
+#pragma unroll
+      for (int m = 0; m < MB; ++m) mx[m] = 0.f;
+      for (int64_t k8 = threadIdx.x; k8 < K / 8; k8 += kThreads) {
+        const int64_t k = 8 * k8;
+        const float4 i0 = *reinterpret_cast<const float4*>(a.inv_s + k);
+        const float4 i1 = *reinterpret_cast<const float4*>(a.inv_s + k + 4);
+        const float inv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+          if (m0 + m >= a.M) continue;
+          const uint4 xr = *reinterpret_cast<const uint4*>(a.X + (m0 + m) * K + k);
+          const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t bits = (e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16);
+            mx[m] = fmaxf(mx[m], fabsf(__fmul_rn(__uint_as_float(bits), inv[e])));
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx[m] = fmaxf(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], o));
+        if (lane == 0) atomicMax(&row_max_bits[m], __float_as_uint(mx[m]));   // non-negative: bit order = value order
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads));
+    float row_down[MB], row_up[MB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+      // smallest shift with max * 2^-shift <= 512: shift = max(0, floor(log2 max) - 8)
+      const int ex = int((row_max_bits[m] >> 23) & 0xFFu) - 127;
+      const int shift = ex > 8 ? (ex - 8 < 120 ? ex - 8 : 120) : 0;
+      row_down[m] = __uint_as_float(uint32_t(127 - shift) << 23);   // 2^-shift
+      row_up[m] = __uint_as_float(uint32_t(127 + shift) << 23);     // 2^shift
+    }
+    // x' = fl32(x * fl32(1 / s)) (times 2^-shift) rounded to fp16, in the paired segment order:
+    // a thread takes 8 channels (one 16-byte load of X) and writes them as one 16-byte word of
+    // a segment
     for (int64_t k8 = threadIdx.x; k8 < K / 8; k8 += kThreads) {
       const int64_t k = 8 * k8;
       const float4 i0 = *reinterpret_cast<const float4*>(a.inv_s + k);
@@ -163,7 +208,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, i
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const uint32_t bits = (e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16);
-          v[e] = __fmul_rn(__uint_as_float(bits), inv[e]);
+          v[e] = __fmul_rn(__fmul_rn(__uint_as_float(bits), inv[e]), row_down[m]);
         }
         // pairs (e, e + 4), e = 0..3; the odd pairs meet codes read as 16 q, so they are stored
         // divided by 16 (exact power-of-two scaling) to keep every product x' (q - z)
@@ -259,7 +304,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, i
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
           if (lane == 0 && m0 + m < a.M) {
             const float b = __uint_as_float(uint32_t(a.bias[n]) << 16);
-            a.Y[(m0 + m) * N + n] = uint16_t(ptx::pack_bf16x2(v + b, 0.f) & 0xFFFFu);
+            a.Y[(m0 + m) * N + n] = uint16_t(ptx::pack_bf16x2(fmaf(v, row_up[m], b), 0.f) & 0xFFFFu);
           }
         }
       }
