@@ -266,6 +266,19 @@ svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void* X_bf16, v
                                           void* stream);
 
 /*
+ * svdq_set_wait_limit -- failure detection.  Every wait inside the kernels (on a barrier that
+ * another warp, the other CTA of a pair or a copy engine completes) gives up after a limit,
+ * records SVDQ_ERR_TIMEOUT in the handle's device error word, finishes or waits out the work it
+ * started and returns, so a lost signal never hangs the GPU.  This call sets that limit for the
+ * handle's later launches (wait_ns nanoseconds; 0 restores the default of two seconds).
+ * stall_kernel = 1 or 2 makes the MMA warp of kernel 1 or kernel 2 wait on a barrier that nothing
+ * completes, so that its wait runs out: the way tests exercise the path without faulting a GPU.
+ * 0 turns it off.  The SVDQuant pages have no counterpart; it is a diagnostics hook.
+ *   Errors: SVDQ_ERR_INVALID_ARG (null handle, stall_kernel outside 0..2).
+ */
+svdq_status_t svdq_set_wait_limit(svdq_handle_t h, uint64_t wait_ns, int32_t stall_kernel);
+
+/*
  * svdq_check_error -- synchronises the handle's device, reads and clears the
  * device error word that the kernels set when a bounded wait gives up.
  * Returns SVDQ_OK or SVDQ_ERR_TIMEOUT (or SVDQ_ERR_CUDA for a sticky CUDA error).

@@ -54,6 +54,8 @@ def test_null_and_bad_arguments():
     assert svdq.LIB.svdq_pack_weights(None, None) == svdq.ERR_INVALID_ARG
     assert svdq.LIB.svdq_destroy(None) == svdq.OK
     assert svdq.LIB.svdq_linear_forward(None, None, None, 4, None) == svdq.ERR_INVALID_ARG
+    assert svdq.LIB.svdq_set_wait_limit(None, 0, 0) == svdq.ERR_INVALID_ARG
+    assert svdq.LIB.svdq_linear_forward_noalloc(None, None, None, 4, None) == svdq.ERR_INVALID_ARG
     W = np.zeros((32, 48), np.uint16)
     with pytest.raises(svdq.SvdqError) as e:
         svdq.pack_host(W, rank=40)                      # rank > min(N, K)

@@ -127,6 +127,10 @@ struct svdq_layer {
   cudaStream_t pipe_in = nullptr, pipe_out = nullptr;
   cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr}, ev_out[2] = {nullptr, nullptr};
   float inv_six = 1.f / 6.f, inv_alpha = 1.f;
+  // failure-detection tests (svdq_set_wait_limit): limit of the kernels' bounded waits, and
+  // which kernel's MMA warp waits on a barrier nothing completes (0 none, 1 kernel 1, 2 kernel 2)
+  uint64_t wait_ns = kDefaultWaitNs;
+  int stall = 0;
 };
 
 namespace {
@@ -301,6 +305,8 @@ svdq_status_t launch_k1(svdq_layer* h, const void* X, int64_t M, void* codes, vo
   a.inv_alpha = h->inv_alpha;
   a.qtab = h->d_qtab;
   a.err = h->d_err;
+  a.wait_ns = h->wait_ns;
+  a.stall = h->stall == 1;
   const K1Plan plan = k1_plan(M, a.K, a.rank, h->sm_count);
   std::string err;
   const int e = k1_launch(a, plan, stream, &err);
@@ -328,6 +334,8 @@ svdq_status_t launch_k2(svdq_layer* h, const void* codes, const void* scales, co
   a.K = K;
   a.rank = int(h->rank_k());
   a.alpha = h->host.alpha;
+  a.wait_ns = h->wait_ns;
+  a.stall = h->stall == 2;
   const int e = k2_launch(maps, a, h->sm_count, stream);
   if (e != 0) return cuda_fail(cudaError_t(e), "kernel 2 launch");
   return SVDQ_OK;
@@ -711,6 +719,14 @@ svdq_status_t svdq_linear_forward_host_batch(svdq_handle_t h, const uint16_t* co
   return SVDQ_OK;
 }
 
+svdq_status_t svdq_set_wait_limit(svdq_handle_t h, uint64_t wait_ns, int32_t stall_kernel) {
+  if (!h) return fail(SVDQ_ERR_INVALID_ARG, "null handle");
+  if (stall_kernel < 0 || stall_kernel > 2) return fail(SVDQ_ERR_INVALID_ARG, "stall_kernel must be 0, 1 or 2");
+  h->wait_ns = wait_ns ? wait_ns : kDefaultWaitNs;
+  h->stall = stall_kernel;
+  return SVDQ_OK;
+}
+
 svdq_status_t svdq_check_error(svdq_handle_t h) {
   if (!h) return fail(SVDQ_ERR_INVALID_ARG, "null handle");
   DeviceGuard guard(h->device);
@@ -808,6 +824,8 @@ extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void
   a.inv_alpha = h->inv_alpha;
   a.qtab = h->d_qtab;
   a.err = h->d_err;
+  a.wait_ns = h->wait_ns;
+  a.stall = h->stall == 1;
   std::string err;
   const int e1 = k1_launch(a, k1_plan(M, a.K, a.rank, h->sm_count), s, &err);
   if (e1 == -1) return fail(SVDQ_ERR_CUDA, err);

@@ -140,10 +140,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, i
                        &full[stage]);
         if (++stage == stages) { stage = 0; phase ^= 1u; }
       }
-      for (int i = 0; i < stages; ++i) {       // every copy issued has landed
+      for (int i = 0; i < stages; ++i) {       // every copy issued has landed, also after an abort
         const int used = issued - i;
         if (used <= 0) continue;
-        bounded_wait(&full[i], uint32_t(((used - 1) / stages) & 1), &abort_flag);
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(&full[i], uint32_t(((used - 1) / stages) & 1)))
+          if (ptx::globaltimer() - t0 > kTimeoutNs) break;
       }
     }
   } else {

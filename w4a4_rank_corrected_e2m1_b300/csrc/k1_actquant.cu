@@ -134,18 +134,28 @@ __device__ __forceinline__ int64_t scale_word_offset(int64_t row, int64_t c, int
   return ((row >> 7) * KG + c) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
 }
 
-__device__ bool k1_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+__device__ bool k1_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, uint64_t limit_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((i & 31u) == 0u) {
       if (*abort_flag) return false;
-      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+      if (ptx::globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(err, 4);
         return false;
       }
+    }
+  }
+}
+// Waits for work already started (ignores the abort flag; gives up after the default limit).
+__device__ void k1_drain(uint64_t* bar, uint32_t parity, int* err) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > kTimeoutNs) {
+      atomicOr(err, 4);
+      return;
     }
   }
 }
@@ -156,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   using C = Cfg<R>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], done;
+  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], done, never;
   __shared__ volatile int abort_flag;
   __shared__ uint32_t tmem_slot;
   __shared__ float s_thr[128], s_rcp[128];
@@ -180,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       ptx::mbar_init(&empty[i], kQWarps + (R > 0 ? 1 : 0));
     }
     ptx::mbar_init(&done, 1);
+    ptx::mbar_init(&never, 1);   // arrived at by nothing (the failure-detection stall waits on it)
     abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -213,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int c = c0; c < nchunks; c += nsplit, ++issued) {
         unsigned char* st = ring + stage * C::STAGE_BYTES;
         if (issued >= pre) {
-          if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err)) break;
+          if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err, a.wait_ns)) break;
           // the quantiser warps read this stage with ordinary loads before releasing it; the
           // proxy fence orders those reads before the tensor copies that overwrite it
           ptx::fence_proxy_async_smem();
@@ -240,8 +251,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t accumulate = 0;
-      for (int c = c0; c < nchunks; c += nsplit) {
-        if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
+      const bool stalled = a.stall && !k1_wait(&never, 0, &abort_flag, a.err, a.wait_ns);
+      for (int c = c0; c < nchunks && !stalled; c += nsplit) {
+        if (!k1_wait(&full[stage], phase, &abort_flag, a.err, a.wait_ns)) break;
         ptx::tc_fence_after();
         const uint32_t xs = ptx::smem_u32(ring + stage * C::STAGE_BYTES);
         const uint32_t ls = xs + C::X_BYTES;
@@ -260,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int stage = 0;
     uint32_t phase = 0;
     for (int c = c0; c < nchunks; c += nsplit) {
-      if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
+      if (!k1_wait(&full[stage], phase, &abort_flag, a.err, a.wait_ns)) break;
       const unsigned char* st = ring + stage * C::STAGE_BYTES;
       // raw bf16 of rows g (w[0]) and g + 8 (w[1]) of this warp, columns 16t .. 16t + 15
       uint32_t w[2][8];
@@ -325,7 +337,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       // TMEM lane quarter = warp: rows 32 warp + lane; column-major partial, so each store of
       // one column by the warp is 128 contiguous bytes
       // a CTA whose K range is empty (more splits than chunks) contributes zeros
-      const bool ok = k1_wait(&done, 0, &abort_flag, a.err) && c0 < nchunks;
+      // the MMAs have completed before TMEM is read (or freed), also after an abort
+      k1_drain(&done, 0, a.err);
+      const bool ok = !abort_flag && c0 < nchunks;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_slot + (uint32_t(32 * warp) << 16);
 #pragma unroll
@@ -479,7 +493,7 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
   constexpr int kProducer = C::PRODUCER, kMma = C::MMA, kQWarps = C::QW;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], done;
+  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], done, never;
   __shared__ volatile int abort_flag;
   __shared__ uint32_t tmem_slot;
   __shared__ float s_thr[128], s_rcp[128];
@@ -500,6 +514,7 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       ptx::mbar_init(&empty[i], kQWarps + (R > 0 ? 1 : 0));
     }
     ptx::mbar_init(&done, 1);
+    ptx::mbar_init(&never, 1);   // arrived at by nothing (the failure-detection stall waits on it)
     abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -530,7 +545,7 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       for (int j = 0; j < nsteps; ++j, ++issued) {
         unsigned char* st = ring + stage * C::STAGE_BYTES;
         if (j >= pre) {
-          if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err)) break;
+          if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err, a.wait_ns)) break;
           ptx::fence_proxy_async_smem();   // ordinary-load reads of the stage before the refill
           ptx::mbar_arrive_expect_tx(&full[stage], C::X_BYTES + C::LI_BYTES);
           tall_li_loads<R>(st + C::X_BYTES, a.LI, j, &full[stage]);
@@ -557,8 +572,9 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t accumulate = 0;
-      for (int j = 0; j < nsteps; ++j) {
-        if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
+      const bool stalled = a.stall && !k1_wait(&never, 0, &abort_flag, a.err, a.wait_ns);
+      for (int j = 0; j < nsteps && !stalled; ++j) {
+        if (!k1_wait(&full[stage], phase, &abort_flag, a.err, a.wait_ns)) break;
         ptx::tc_fence_after();
         const uint32_t xs = ptx::smem_u32(ring + stage * C::STAGE_BYTES);
         const uint32_t ls = xs + C::X_BYTES;
@@ -601,7 +617,7 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     for (int j = 0; j < nsteps; ++j, code_p += C::CH * 32, scale_p += C::CH * 512) {
-      if (!k1_wait(&full[stage], phase, &abort_flag, a.err)) break;
+      if (!k1_wait(&full[stage], phase, &abort_flag, a.err, a.wait_ns)) break;
       const unsigned char* st = ring + stage * C::STAGE_BYTES;
       uint32_t w[8];
       float il[16];
@@ -677,7 +693,9 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       float* red = reinterpret_cast<float*>(ring);   // [3][r][32 lanes]
       if (warp < kQWarps) ptx::bar_sync(1, 32 * kQWarps);
       if (warp < 4) {
-        const bool ok = k1_wait(&done, 0, &abort_flag, a.err);
+        // the MMAs have completed before TMEM is read (or freed), also after an abort
+        k1_drain(&done, 0, a.err);
+        const bool ok = !abort_flag;
         ptx::tc_fence_after();
         if (warp > 0) {
 #pragma unroll
@@ -702,8 +720,10 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
         }
       }
     } else if (warp == 0) {
-      // one product per chunk: T is TMEM lanes 0..31
-      const bool ok = k1_wait(&done, 0, &abort_flag, a.err);
+      // one product per chunk: T is TMEM lanes 0..31 (read once the MMAs have completed, also
+      // after an abort)
+      k1_drain(&done, 0, a.err);
+      const bool ok = !abort_flag;
       ptx::tc_fence_after();
 #pragma unroll
       for (int cb = 0; cb < R; cb += 32) {

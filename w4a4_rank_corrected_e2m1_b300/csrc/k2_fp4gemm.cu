@@ -88,18 +88,19 @@ struct Smem {
   uint64_t acc_full;         // accumulator ready for this CTA's epilogue (MMA commit, multicast)
   uint64_t acc_empty;        // even CTA: both epilogues drained the accumulator (16 warps)
   uint64_t drain;            // even CTA: every MMA issued has completed
+  uint64_t never;            // arrived at by nothing (the failure-detection stall waits on it)
   uint32_t tmem_base;
   volatile int abort_flag;
 };
 
-__device__ bool wait_bounded(uint64_t* bar, uint32_t parity, Smem* s, int* err) {
+__device__ bool wait_bounded(uint64_t* bar, uint32_t parity, Smem* s, int* err, uint64_t limit_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((i & 31u) == 0u) {
       if (s->abort_flag) return false;
-      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+      if (ptx::globaltimer() - t0 > limit_ns) {
         s->abort_flag = 1;
         atomicOr(err, 1);
         return false;
@@ -182,6 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     ptx::mbar_init(&s->acc_full, 1);
     ptx::mbar_init(&s->acc_empty, 2 * EPI_WARPS);
     ptx::mbar_init(&s->drain, 1);
+    ptx::mbar_init(&s->never, 1);
     s->abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -255,7 +257,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           unsigned char* st = stages + stage * STAGE_BYTES;
           uint64_t* fb = &s->full[stage];
           if (!(tile == pair && it < pre)) {
-            if (!wait_bounded(&s->empty[stage], phase ^ 1u, s, a.err)) { ok = false; break; }
+            if (!wait_bounded(&s->empty[stage], phase ^ 1u, s, a.err, a.wait_ns)) { ok = false; break; }
             // No proxy fence is needed before overwriting the stage: the scale warps' ordinary
             // loads of its scales have completed before the stage is released (their values
             // went into tcgen05.st and tcgen05.wait::st returned before the warps arrived on
@@ -274,14 +276,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = true;
+      bool ok = !(a.stall && !wait_bounded(&s->never, 0, s, a.err, a.wait_ns));
       int local = 0;
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++local) {
-        if (!wait_bounded(&s->acc_empty, (uint32_t(local) & 1u) ^ 1u, s, a.err)) break;
+        if (!wait_bounded(&s->acc_empty, (uint32_t(local) & 1u) ^ 1u, s, a.err, a.wait_ns)) break;
         ptx::tc_fence_after();
         uint32_t accumulate = 0;
         for (int it = 0; it < iters; ++it) {
-          if (!wait_bounded(&s->ready[stage], phase, s, a.err)) { ok = false; break; }
+          if (!wait_bounded(&s->ready[stage], phase, s, a.err, a.wait_ns)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t a_s = ptx::smem_u32(stages + stage * STAGE_BYTES);
           const uint32_t b_s = a_s + A_BYTES;
@@ -335,7 +337,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
       for (int it = 0; it < iters; ++it) {
-        if (!wait_bounded(&s->full[stage], phase, s, a.err)) { ok = false; break; }
+        if (!wait_bounded(&s->full[stage], phase, s, a.err, a.wait_ns)) { ok = false; break; }
         if (it >= n_lr) {
           // A scales: the MMA reads row 32q + lane from this lane, column base + 4 kk + q; the
           // row's four scales of k-step kk are the word at kk * 512 + lane * 16 + q * 4 of the
@@ -389,7 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         *reinterpret_cast<uint2*>(my_bias + 4 * lane) = v;
         __syncwarp();
       }
-      if (!wait_bounded(&s->acc_full, uint32_t(local) & 1u, s, a.err)) break;
+      if (!wait_bounded(&s->acc_full, uint32_t(local) & 1u, s, a.err, a.wait_ns)) break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * half);
       uint32_t r[64], o[32];

@@ -90,6 +90,8 @@ struct K1Args {
   float s_gX, inv_six, inv_alpha;
   const float* qtab;          // 256 floats: E4M3 scale thresholds [0,128), reciprocals [128,256)
   int* err;                   // device error word (bounded waits)
+  uint64_t wait_ns;           // limit of every bounded wait (nanoseconds)
+  int stall;                  // failure-detection tests: the MMA warp waits on a barrier nothing completes
 };
 struct K1Plan {
   bool tall = false;          // 32-row tiles over the whole of K (no split) instead of 128-row split tiles
@@ -119,7 +121,11 @@ struct K2Args {
   int64_t M, N, K;
   int rank;
   float alpha;
+  uint64_t wait_ns;           // limit of every bounded wait (nanoseconds)
+  int stall;                  // failure-detection tests: the MMA thread waits on a barrier nothing completes
 };
+// Default limit of the kernels' bounded waits: two seconds.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 int k2_launch(const K2Maps& maps, const K2Args& a, int sm_count, void* stream);
 size_t k2_smem_bytes();
 

@@ -83,6 +83,7 @@ _SIGS = {
     "svdq_linear_forward_host_batch": (_i32, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _vp]),
     "svdq_linear_forward_noalloc": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_check_error": (_i32, [_vp]),
+    "svdq_set_wait_limit": (_i32, [_vp, ctypes.c_uint64, _i32]),
     "svdq_attach_lora": (_i32, [_vp, _vp, _vp, _i64, ctypes.c_float, _vp]),
     "svdq_awq_pack_host": (_i32, [ctypes.POINTER(AwqParams), ctypes.POINTER(AwqHost)]),
     "svdq_awq_pack": (_i32, [ctypes.POINTER(AwqParams), ctypes.POINTER(_vp)]),
@@ -286,6 +287,11 @@ class Layer:
 
     def check_error(self):
         check(LIB.svdq_check_error(self.h), "svdq_check_error")
+
+    def set_wait_limit(self, wait_ns: int = 0, stall_kernel: int = 0):
+        """Limit of the kernels' bounded waits (0 = default) and the failure-detection stall
+        (0 none, 1 kernel 1, 2 kernel 2)."""
+        check(LIB.svdq_set_wait_limit(self.h, wait_ns, stall_kernel), "svdq_set_wait_limit")
 
     def attach_lora(self, A, B, scale: float = 1.0, stream=None):
         """Append a LoRA adapter (A: K x r_lora, B: r_lora x N, bf16 bit patterns on the host)
