@@ -8,8 +8,9 @@ The CUDA library never calls it and shares no code with it.
 
 Modules:
   nvfp4     -- E2M1 / E4M3 encodings and the 16-element block quantiser
+  int4      -- the INT4 variant's 64-element group quantiser
   svdquant  -- smoothing, low-rank split, residual quantisation, forward pass
 
 Parity status of each function is listed in the module headers.
 """
-from . import nvfp4, svdquant  # noqa: F401
+from . import int4, nvfp4, svdquant  # noqa: F401

@@ -35,6 +35,9 @@ Eckart-Young (residual energy equals the tail of the spectrum computed through
 an eigen-decomposition); full rank leaves R = 0; lambda = 1 with r = 0 equals
 plain W4A4 quantisation of X and W; a pure-Python loop evaluation of the
 forward on 4 x 16 x 16; SVDQuant beats naive W4A4 on outlier-heavy inputs.
+The INT4 variant (pack_int4, quantize_act_int4, forward_int4) shares every step up to the
+residual and quantises with oracle.int4 instead; its pins mirror the NVFP4 ones (reduction to
+plain INT4 W4A4 at lambda = 1 and r = 0, loops on a tiny case, the method claim on outliers).
 Image-quality and end-to-end speed claims of the pages: parity unpinned (they
 need trained models).
 """
@@ -42,7 +45,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import nvfp4
+from . import int4, nvfp4
 
 
 # ----------------------------------------------------------------------------- formats
@@ -108,14 +111,9 @@ def residual(What, L1_bits, L2_bits) -> np.ndarray:
     return (What - (L1 @ L2).T).astype(np.float32)
 
 
-def pack(W_bits, bias_bits, rank, Xcal_bits=None, smooth=True, L1_bits=None, L2_bits=None):
-    """Offline step: smoothing, low-rank split, residual quantisation.
-
-    Returns a dict of the packed layer in canonical layouts:
-      inv_lambda (K fp32), lam (K fp32), L1 (K x r bf16 bits), L2 (r x N bf16 bits),
-      R_codes (N x K uint8 nibbles), R_scales (N x K/16 E4M3 bits), s_gW, s_gX (fp32),
-      bias (N bf16 bits), R (N x K fp32).
-    """
+def split(W_bits, rank, Xcal_bits=None, smooth=True, L1_bits=None, L2_bits=None):
+    """Stages one to three up to the residual: lambda, inv_lambda, the bf16 factors and the
+    float32 residual R (shared by the NVFP4 and the INT4 variants)."""
     N, K = W_bits.shape
     if smooth and Xcal_bits is not None:
         lam, inv = smoothing_factors(Xcal_bits, W_bits)
@@ -127,6 +125,19 @@ def pack(W_bits, bias_bits, rank, Xcal_bits=None, smooth=True, L1_bits=None, L2_
         L1, L2, _ = lowrank_factors(What, rank)
         L1_bits, L2_bits = f64_to_bf16(L1), f64_to_bf16(L2)
     R = residual(What, L1_bits, L2_bits)
+    return lam, inv, np.asarray(L1_bits, np.uint16), np.asarray(L2_bits, np.uint16), R
+
+
+def pack(W_bits, bias_bits, rank, Xcal_bits=None, smooth=True, L1_bits=None, L2_bits=None):
+    """Offline step: smoothing, low-rank split, residual quantisation.
+
+    Returns a dict of the packed layer in canonical layouts:
+      inv_lambda (K fp32), lam (K fp32), L1 (K x r bf16 bits), L2 (r x N bf16 bits),
+      R_codes (N x K uint8 nibbles), R_scales (N x K/16 E4M3 bits), s_gW, s_gX (fp32),
+      bias (N bf16 bits), R (N x K fp32).
+    """
+    N, K = W_bits.shape
+    lam, inv, L1_bits, L2_bits, R = split(W_bits, rank, Xcal_bits, smooth, L1_bits, L2_bits)
     s_gW = nvfp4.global_scale(np.max(np.abs(R)) if R.size else 0.0)
     codes, scales = nvfp4.quantize_blocks(R, s_gW)
     if Xcal_bits is not None:
@@ -135,10 +146,22 @@ def pack(W_bits, bias_bits, rank, Xcal_bits=None, smooth=True, L1_bits=None, L2_
         s_gX = np.float32(1.0)
     if bias_bits is None:
         bias_bits = np.zeros(N, np.uint16)
-    return dict(lam=lam, inv_lambda=inv, L1=np.asarray(L1_bits, np.uint16),
-                L2=np.asarray(L2_bits, np.uint16), R=R, R_codes=codes, R_scales=scales,
+    return dict(lam=lam, inv_lambda=inv, L1=L1_bits, L2=L2_bits, R=R, R_codes=codes, R_scales=scales,
                 s_gW=np.float32(s_gW), s_gX=np.float32(s_gX), bias=np.asarray(bias_bits, np.uint16),
                 rank=int(rank))
+
+
+def pack_int4(W_bits, bias_bits, rank, Xcal_bits=None, smooth=True, L1_bits=None, L2_bits=None):
+    """The INT4 variant's offline step: the same smoothing, low-rank split and residual, then R
+    quantised to INT4 groups (oracle.int4): R_codes (N x K nibbles q + 8), R_scales (N x K/64
+    float32).  No global scales."""
+    N, K = W_bits.shape
+    lam, inv, L1_bits, L2_bits, R = split(W_bits, rank, Xcal_bits, smooth, L1_bits, L2_bits)
+    codes, scales = int4.quantize_groups(R)
+    if bias_bits is None:
+        bias_bits = np.zeros(N, np.uint16)
+    return dict(fmt="int4", lam=lam, inv_lambda=inv, L1=L1_bits, L2=L2_bits, R=R, R_codes=codes,
+                R_scales=scales, bias=np.asarray(bias_bits, np.uint16), rank=int(rank))
 
 
 # ----------------------------------------------------------------------------- step 4
@@ -165,6 +188,23 @@ def forward(X_bits, p):
     Xdq = nvfp4.dequantize_blocks(cx, sx)
     Rdq = nvfp4.dequantize_blocks(p["R_codes"], p["R_scales"])
     Y = np.float64(alpha(p)) * (Xdq @ Rdq.T)
+    if p["rank"]:
+        Y += lowrank_down(xh, p["L1"]) @ bf16_to_f64(p["L2"])
+    return Y + bf16_to_f64(p["bias"])[None, :]
+
+
+def quantize_act_int4(X_bits, inv32):
+    """The INT4 variant's run-time activation quantisation: x^ = fl32(x inv_lambda), then INT4
+    groups of 64 with a float32 scale each (oracle.int4)."""
+    xh = smooth_act(X_bits, inv32)
+    codes, scales = int4.quantize_groups(xh)
+    return codes, scales, xh
+
+
+def forward_int4(X_bits, p):
+    """Y = deq(Q4i(X^)) deq(Q4i(R))^T + (X^ L1) L2 + b in float64 for the INT4 variant."""
+    cx, sx, xh = quantize_act_int4(np.asarray(X_bits), p["inv_lambda"])
+    Y = int4.dequantize_groups(cx, sx) @ int4.dequantize_groups(p["R_codes"], p["R_scales"]).T
     if p["rank"]:
         Y += lowrank_down(xh, p["L1"]) @ bf16_to_f64(p["L2"])
     return Y + bf16_to_f64(p["bias"])[None, :]

@@ -205,3 +205,70 @@ def test_lora_delta_rows_subset_matches_full():
     full = sq.lora_delta(X, A, B, 0.5)
     rows = np.array([0, 4, 8])
     assert np.array_equal(sq.lora_delta(X, A, B, 0.5, rows=rows), full[rows])
+
+
+# ----------------------------------------------------------------------------- INT4 variant
+def _naive_int4(X_bits, W_bits, bias_bits):
+    """Plain INT4 W4A4 (64-element groups) without smoothing or low-rank branch."""
+    from oracle import int4
+    cx, sx = int4.quantize_groups(sq.bf16_to_f32(X_bits))
+    cw, sw = int4.quantize_groups(sq.bf16_to_f32(W_bits))
+    return int4.dequantize_groups(cx, sx) @ int4.dequantize_groups(cw, sw).T + sq.bf16_to_f64(bias_bits)[None, :]
+
+
+def test_int4_unsmoothed_rank0_is_plain_int4(tiny):
+    from oracle import int4
+    w, d = tiny
+    p = sq.pack_int4(d["W"], d["bias"], 0, Xcal_bits=None, smooth=False)
+    wf = sq.bf16_to_f32(d["W"])
+    cw, sw = int4.quantize_groups(wf)
+    assert np.array_equal(p["R"], wf)
+    assert np.array_equal(p["R_codes"], cw) and np.array_equal(p["R_scales"], sw)
+    assert np.allclose(sq.forward_int4(d["X"], p), _naive_int4(d["X"], d["W"], d["bias"]), rtol=0, atol=1e-12)
+
+
+def test_int4_forward_against_python_loops():
+    """3 x 128 x 5 and 2 x 64 x 4: the INT4 forward as explicit scalar loops, group by group:
+    the integer dot product of each 64-element group scaled by its two scales."""
+    for (M, K, N, r) in [(3, 128, 5, 2), (2, 64, 4, 1)]:
+        w = synthetic.scaled(synthetic.TINY, M=M, K=K, N=N, rank=r, n_outlier=1, spike_rank=1)
+        d = synthetic.make(w, seed=9)
+        p = sq.pack_int4(d["W"], d["bias"], r, Xcal_bits=d["X"])
+        Y = sq.forward_int4(d["X"], p)
+        cx, sx, xh = sq.quantize_act_int4(d["X"], p["inv_lambda"])
+        L1 = sq.bf16_to_f64(p["L1"])
+        L2 = sq.bf16_to_f64(p["L2"])
+        b = sq.bf16_to_f64(p["bias"])
+        for m in range(M):
+            for n in range(N):
+                acc = 0.0
+                for g in range(K // 64):
+                    isum = 0
+                    for k in range(64 * g, 64 * g + 64):
+                        isum += (int(cx[m, k]) - 8) * (int(p["R_codes"][n, k]) - 8)
+                    acc += float(sx[m, g]) * float(p["R_scales"][n, g]) * isum
+                lr = 0.0
+                for j in range(r):
+                    t = 0.0
+                    for k in range(K):
+                        t += float(xh[m, k]) * L1[k, j]
+                    lr += t * L2[j, n]
+                assert abs(acc + lr + b[n] - Y[m, n]) <= 1e-9 * (1 + abs(Y[m, n]))
+
+
+def test_int4_full_rank_reproduces_product(tiny):
+    w, d = tiny
+    p = sq.pack_int4(d["W"], d["bias"], w.K, Xcal_bits=d["X"])
+    Y = sq.forward_int4(d["X"], p)
+    assert sq.rel_fro(Y, sq.exact_product(d["X"], d["W"], d["bias"])) < 2e-3
+
+
+@pytest.mark.parametrize("name", ["tiny", "qkv_small"])
+def test_int4_svdquant_beats_naive_int4_on_outliers(name):
+    w = {c.name: c for c in synthetic.parity_cases()}[name]
+    d = synthetic.make(w)
+    ref = sq.exact_product(d["X"], d["W"], d["bias"])
+    p = sq.pack_int4(d["W"], d["bias"], w.rank, Xcal_bits=d["X"])
+    e_svdq = sq.rel_fro(sq.forward_int4(d["X"], p), ref)
+    e_naive = sq.rel_fro(_naive_int4(d["X"], d["W"], d["bias"]), ref)
+    assert e_svdq < e_naive, (e_svdq, e_naive)
