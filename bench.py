@@ -409,6 +409,47 @@ def point_summary(w, t, hbm, fp4_peak):
     }
 
 
+def measure_int4(torch, svdq, w, pt, stream, flush, bf16_peak, reps=50, warm=5):
+    """The INT4 variant of the same layer (svdq_int4_forward and its activation kernel alone) on
+    the headline workload: medians with cold and warm L2.  Its GEMM runs bf16 warp MMAs on
+    unpacked INT4 codes, so the fraction is against the measured bf16 tensor peak."""
+    M, K = w.M, w.K
+    layer = svdq.Int4Layer(pt.d["W"], w.rank, bias=pt.d["bias"], Xcal=pt.d["X"], M_max=M)
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((K // 64, svdq.int4_scale_ld(M)), dtype=torch.float32, device="cuda")
+    T = torch.empty((M, max(layer.r_pad, 8)), dtype=torch.int16, device="cuda")
+    nb = len(pt.Xs)
+
+    def fwd(i, ev):
+        if ev:
+            ev[0].record(stream)
+        layer.forward(pt.Xs[i % nb], pt.Y, M, stream)
+        if ev:
+            ev[1].record(stream)
+
+    def k1(i, ev):
+        if ev:
+            ev[0].record(stream)
+        layer.quantize_act(pt.Xs[i % nb], M, codes, scales, T, stream)
+        if ev:
+            ev[1].record(stream)
+
+    out = {}
+    for mode, fl in (("cold_l2", flush), ("warm_l2", None)):
+        f = time_events(torch, stream, fwd, reps, warm, fl, 2)
+        k = time_events(torch, stream, k1, reps, warm, fl, 2)
+        out[mode] = {"fwd_us": round(1e3 * statistics.median(r[0] for r in f), 2),
+                     "k1_us": round(1e3 * statistics.median(r[0] for r in k), 2)}
+    layer.check_error()
+    layer.close()
+    t = out["cold_l2"]["fwd_us"] * 1e-6
+    tflops = workload_flops(w) / t / 1e12
+    out.update(workload=w.name, tflops=tflops, tokens_per_s=M / t, frac_bf16_peak=tflops / bf16_peak,
+               note="INT4 groups of 64 (float32 scales); GEMM on bf16 warp MMAs over unpacked codes; "
+                    "fraction of the measured bf16 tensor peak")
+    return out
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -481,7 +522,9 @@ def run_ours(args, w):
     # ---- every other timed point of the scope table (one GPU only: the scaling runs time the
     # headline alone)
     sweep = {}
+    int4 = None
     if world == 1 and not args.no_sweep:
+        int4 = measure_int4(torch, svdq, w, pt, stream, flush, bf16)
         for sw in synthetic.SWEEP:
             if sw.name == w.name:
                 sweep[sw.name] = point_summary(sw, t, hbm, fp4_peak)
@@ -531,6 +574,8 @@ def run_ours(args, w):
             "clocks": clk,
             "pack_s": pt.pack_s,
         }
+        if int4:
+            out["int4_variant"] = int4
         if sweep:
             out["sweep"] = sweep
             out["sweep_note"] = ("per point: medians of 100 CUDA-event timings after 10 warm-ups; cold_l2 = "

@@ -289,6 +289,82 @@ const char* svdq_status_string(svdq_status_t s);
 const char* svdq_last_error(void);
 
 /* ==================================================================================
+ * INT4 variant of the SVDQuant layer
+ *
+ * The pages say SVDQuant supports both INT4 and FP4 and that Nunchaku runs INT4 kernels on
+ * hardware older than Blackwell (aiflownews article on Nunchaku, "What SVDQuant actually does",
+ * "How Nunchaku four bit quantization actually works"); they give no INT4 group size or scale
+ * format.  Reading used here: the same smoothing, low-rank branch and residual as the NVFP4
+ * layer, with the residual and the smoothed activations quantised to symmetric INT4 groups:
+ *   q = clamp(rint(fl32(v * fl32(1 / s))), -7, 7), ties to even, s = fl32(amax / 7) per 64
+ *   consecutive elements along K (s = 0 and q = 0 for an all-zero group),
+ *   Y = sum_g sX[m, g] sW[n, g] (sum_{k in g} qx qw) + (X^ L1) L2 + b,   bf16 out.
+ * This part's tensor cores have no integer MMA of the tcgen05 family, and the per-group scales
+ * sit inside the K sum, so the GEMM unpacks the codes to bf16 and runs warp-level MMAs, finishing
+ * each group's exact integer sum in float32 registers before scaling it.
+ * Layouts:
+ *   codes    rows x K/2 bytes, element k in byte k/2 (low nibble for even k), nibble = q + 8.
+ *   scales   device: group-major float32, [K/64][svdq_int4_scale_ld(rows)] (scale of row m, group
+ *            g at g * ld + m; rows past the last are padding); host export: rows x K/64 row-major.
+ *   T        rows x r_pad bf16, T = X^ L1 (not divided by anything), r_pad = 64 * ceil(rank / 64).
+ * Shape rules: K % 64 == 0, N % 16 == 0, rank % 16 == 0, 0 <= rank <= min(128, N, K).
+ * ================================================================================== */
+typedef struct svdq_int4_layer* svdq_int4_handle_t;
+
+/* The packed INT4 layer in canonical host layouts (caller-allocated buffers, NULL = skip). */
+typedef struct {
+  float* lambda;        /* K                                                   */
+  float* inv_lambda;    /* K                                                   */
+  uint16_t* L1_bf16;    /* K x rank                                            */
+  uint16_t* L2_bf16;    /* rank x N                                            */
+  uint8_t* R_codes;     /* N x K/2                                             */
+  float* R_scales;      /* N x K/64, row-major                                 */
+  uint16_t* bias_bf16;  /* N                                                   */
+} svdq_int4_host_t;
+
+/* Rows of a group-major scale buffer for `rows` rows: 128 * ceil(rows / 128). */
+int64_t svdq_int4_scale_ld(int64_t rows);
+
+/*
+ * svdq_int4_pack_host -- the INT4 offline step on the CPU (no CUDA call): smoothing, the
+ * randomized top-rank SVD, the residual against the bf16 factors, INT4 groups.  Uses the fields
+ * of svdq_pack_params_t as svdq_pack_host does (s_gX is ignored: the INT4 groups need no global
+ * scale).  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, OOM.
+ */
+svdq_status_t svdq_int4_pack_host(const svdq_pack_params_t* p, svdq_int4_host_t* out);
+
+/*
+ * svdq_int4_pack -- svdq_int4_pack_host, then the device layouts uploaded to p->device
+ * (synchronised before return); reserves a workspace for M <= p->M_max when M_max > 0.
+ * Errors: those of svdq_int4_pack_host, ARCH, OOM, CUDA.
+ */
+svdq_status_t svdq_int4_pack(const svdq_pack_params_t* p, svdq_int4_handle_t* out);
+svdq_status_t svdq_int4_export(svdq_int4_handle_t h, svdq_int4_host_t* out);
+
+/* Library-owned workspace for svdq_int4_forward with M <= M_max (replaces any earlier one). */
+svdq_status_t svdq_int4_reserve(svdq_int4_handle_t h, int64_t M_max);
+
+/*
+ * svdq_int4_quantize_act -- kernel int4_k1 alone: x^ = fl32(x * inv_lambda), INT4 groups of x^
+ * (bit-exact with the quantiser above) and T = X^ L1 (float32 accumulation, bf16 out).
+ * X: device M x K bf16; x_codes: device M x K/2; x_scales: device float32 group-major with
+ * ld = svdq_int4_scale_ld(M); T: device M x r_pad bf16 (NULL when rank == 0).  16-byte aligned.
+ */
+svdq_status_t svdq_int4_quantize_act(svdq_int4_handle_t h, const void* X_bf16, int64_t M, void* x_codes,
+                                     float* x_scales, void* T_bf16, void* stream);
+
+/*
+ * svdq_int4_forward -- the INT4 layer: kernel int4_k1 then kernel int4_k2 on `stream`.
+ * X: device M x K bf16; Y: device M x N bf16, fully overwritten.  X, Y and the workspace must
+ * not overlap.  Errors: INVALID_ARG, WORKSPACE (no workspace for M), CUDA.
+ */
+svdq_status_t svdq_int4_forward(svdq_int4_handle_t h, const void* X_bf16, void* Y_bf16, int64_t M, void* stream);
+
+/* Synchronises, reads and clears the device error word (SVDQ_ERR_TIMEOUT if a wait gave up). */
+svdq_status_t svdq_int4_check_error(svdq_int4_handle_t h);
+svdq_status_t svdq_int4_destroy(svdq_int4_handle_t h);
+
+/* ==================================================================================
  * AWQ-style W4A16 linear layer (the modulation / adaptive-normalisation layers)
  *
  * The pages keep 16-bit activations and quantise only the weights to four bits, AWQ style,

@@ -114,6 +114,47 @@ def test_host_quantizer_on_hand_worked_and_edge_rows():
     assert np.array_equal(got["R_scales"], sw)
 
 
+# ------------------------------------------------------------------ INT4 variant host pack
+def _pack_nibbles(c):
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("case", ["tiny", "qkv_small", "down_small"])
+def test_int4_host_pack_bit_exact_with_oracle_factors(case):
+    w = {c.name: c for c in synthetic.parity_cases()}[case]
+    d = synthetic.make(w)
+    ref = sq.pack_int4(d["W"], d["bias"], w.rank, Xcal_bits=d["X"])
+    got = svdq.int4_pack_host(d["W"], w.rank, bias=d["bias"], Xcal=d["X"], L1=ref["L1"], L2=ref["L2"])
+    assert np.array_equal(got["lam"], ref["lam"]) and np.array_equal(got["inv_lambda"], ref["inv_lambda"])
+    assert np.array_equal(got["R_codes"], _pack_nibbles(ref["R_codes"]))
+    assert np.array_equal(got["R_scales"].view(np.uint32), ref["R_scales"].view(np.uint32))
+    assert np.array_equal(got["bias"], ref["bias"])
+
+
+def test_int4_host_quantizer_on_edge_rows():
+    """Zero groups, ties, negative zeros and wide magnitude ranges through the library's INT4
+    quantiser (lambda = 1, rank 0: R = W exactly) against the oracle's."""
+    from oracle import int4
+    rng = np.random.default_rng(12)
+    rows = [[0.0] * 128, ([7, -7, 2.5, -2.5, 3.5, -3.5, 0.5, -0.5, -0.0, 1.5] + [0.0] * 54) * 2]
+    rows += [list(rng.standard_normal(128) * 10 ** rng.uniform(-4, 4)) for _ in range(30)]
+    W = synthetic.f64_to_bf16_bits(np.array(rows, np.float64))
+    got = svdq.int4_pack_host(W, 0, smooth=False)
+    cw, sw = int4.quantize_groups(sq.bf16_to_f32(W))
+    assert np.array_equal(got["R_codes"], _pack_nibbles(cw))
+    assert np.array_equal(got["R_scales"].view(np.uint32), sw.view(np.uint32))
+
+
+def test_int4_shape_errors():
+    W = np.zeros((32, 96), np.uint16)                 # K % 64 != 0
+    with pytest.raises(svdq.SvdqError) as e:
+        svdq.int4_pack_host(W, 0)
+    assert e.value.status == svdq.ERR_UNSUPPORTED_SHAPE
+    assert svdq.LIB.svdq_int4_forward(None, None, None, 4, None) == svdq.ERR_INVALID_ARG
+    assert svdq.LIB.svdq_int4_destroy(None) == svdq.OK
+    assert svdq.int4_scale_ld(1) == 128 and svdq.int4_scale_ld(129) == 256
+
+
 @pytest.mark.parametrize("shape", [(256, 256, 16), (512, 768, 32), (384, 1024, 64)])
 def test_randomized_svd_near_eckart_young(shape):
     N, K, r = shape

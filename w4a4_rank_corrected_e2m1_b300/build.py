@@ -24,9 +24,9 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-
                      "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 CXX_FLAGS = ["-O3", "-std=c++17", "-fPIC", "-fopenmp", "-ffp-contract=off", "-I", os.path.join(ROOT, "include")]
 
-CU_SOURCES = ["api.cu", "k1_actquant.cu", "k2_fp4gemm.cu", "awq_gemv.cu"]
+CU_SOURCES = ["api.cu", "k1_actquant.cu", "k2_fp4gemm.cu", "awq_gemv.cu", "int4_path.cu", "int4_api.cu"]
 CXX_SOURCES = ["pack_host.cpp", "awq_host.cpp"]
-HEADERS = ["svdq_internal.h", "ptx.cuh"]
+HEADERS = ["svdq_internal.h", "ptx.cuh", "abi_util.cuh"]
 
 
 def _nvcc() -> str:

@@ -18,49 +18,36 @@
 #include <string>
 #include <vector>
 
+#include "abi_util.cuh"
 #include "svdq_internal.h"
 
 using namespace svdq;
 
 namespace {
 
-thread_local std::string g_last_error;
-
-svdq_status_t fail(svdq_status_t s, const std::string& msg) {
-  g_last_error = msg;
-  return s;
-}
-svdq_status_t cuda_fail(cudaError_t e, const char* what) {
-  return fail(SVDQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
-}
-
-struct DeviceGuard {
-  int prev = -1;
-  bool changed = false;
-  explicit DeviceGuard(int dev) {
-    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
-      changed = cudaSetDevice(dev) == cudaSuccess;
-    }
-  }
-  ~DeviceGuard() {
-    if (changed) cudaSetDevice(prev);
-  }
-};
-
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-
-void* dalloc(size_t bytes, cudaError_t* e) {
-  void* p = nullptr;
-  *e = cudaMalloc(&p, bytes ? bytes : 256);
-  return *e == cudaSuccess ? p : nullptr;
-}
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
 namespace svdq {
+
+std::string& last_error_slot() {
+  thread_local std::string msg;
+  return msg;
+}
+
+svdq_status_t check_arch(int device) {
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(SVDQ_ERR_ARCH, "device " + std::to_string(device) + " is sm_" + std::to_string(prop.major) +
+                                   std::to_string(prop.minor) + ", this library is built for sm_103a (B300)");
+  return SVDQ_OK;
+}
 
 bool encode_map_2d(void* map, int dtype_bytes, const void* base, uint64_t inner, uint64_t outer,
                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle128,
@@ -77,7 +64,9 @@ bool encode_map_2d(void* map, int dtype_bytes, const void* base, uint64_t inner,
     *err = "cuTensorMapEncodeTiled is not available from the driver";
     return false;
   }
-  const CUtensorMapDataType dt = dtype_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = dtype_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : dtype_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[2] = {inner, outer < 1 ? 1 : outer};
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
@@ -159,15 +148,6 @@ WsLayout ws_layout(const svdq_layer* h, int64_t M, int staging) {
   return w;
 }
 
-svdq_status_t check_arch(int device) {
-  cudaDeviceProp prop;
-  cudaError_t e = cudaGetDeviceProperties(&prop, device);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
-  if (!(prop.major == 10 && prop.minor == 3))
-    return fail(SVDQ_ERR_ARCH, "device " + std::to_string(device) + " is sm_" + std::to_string(prop.major) +
-                                   std::to_string(prop.minor) + ", this library is built for sm_103a (B300)");
-  return SVDQ_OK;
-}
 
 svdq_status_t check_shape(int64_t N, int64_t K, int64_t r) {
   if (K % 64 != 0 || N % 16 != 0 || r < 0 || r > 128 || r % 16 != 0 || r > std::min(N, K))
@@ -341,13 +321,6 @@ svdq_status_t launch_k2(svdq_layer* h, const void* codes, const void* scales, co
   return SVDQ_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
-bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
-  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return na > 0 && nb > 0 && x < y + nb && y < x + na;
-}
 
 }  // namespace
 
@@ -367,7 +340,7 @@ const char* svdq_status_string(svdq_status_t s) {
   return "unknown status";
 }
 
-const char* svdq_last_error(void) { return g_last_error.c_str(); }
+const char* svdq_last_error(void) { return last_error_slot().c_str(); }
 
 int64_t svdq_scales_bytes(int64_t M, int64_t K) {
   if (M < 0 || K < 0) return 0;

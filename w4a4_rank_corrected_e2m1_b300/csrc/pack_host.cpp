@@ -319,7 +319,33 @@ void randomized_lowrank(const double* What, int64_t N, int64_t K, int64_t r, int
 }  // namespace
 
 // ------------------------------------------------------------------ pack
-svdq_status_t pack_on_host(const svdq_pack_params_t* p, HostPack* out, std::string* err) {
+// INT4 group quantiser of the INT4 variant, per 64 elements: s = fl32(amax / 7), q =
+// clamp(rint(fl32(v * fl32(1 / s))), -7, 7) (ties to even), stored as the nibble q + 8 (element
+// k in byte k / 2, low nibble for even k); an all-zero group has s = 0 and q = 0.
+void int4_quantize_row(const float* v, int64_t K, uint8_t* codes, float* scales) {
+  for (int64_t g = 0; g < K / 64; ++g) {
+    float amax = 0.f;
+    for (int i = 0; i < 64; ++i) amax = std::max(amax, std::fabs(v[64 * g + i]));
+    const float s = amax / 7.0f;
+    scales[g] = s;
+    const float rcp = s > 0.f ? 1.0f / s : 0.f;
+    for (int i = 0; i < 64; i += 2) {
+      uint8_t byte = 0;
+      for (int h = 0; h < 2; ++h) {
+        int q = 0;
+        if (s > 0.f) {
+          const float t = v[64 * g + i + h] * rcp;
+          q = int(std::nearbyint(t));
+          q = q < -7 ? -7 : (q > 7 ? 7 : q);
+        }
+        byte |= uint8_t(q + 8) << (4 * h);
+      }
+      codes[(64 * g + i) / 2] = byte;
+    }
+  }
+}
+
+svdq_status_t pack_on_host(const svdq_pack_params_t* p, HostPack* out, std::string* err, std::vector<float>* R_keep) {
   if (!p || !out) { *err = "null argument"; return SVDQ_ERR_INVALID_ARG; }
   const int64_t N = p->N, K = p->K, r = p->rank;
   if (N <= 0 || K <= 0 || r < 0 || !p->W_bf16) { *err = "N, K must be > 0, rank >= 0, W required"; return SVDQ_ERR_INVALID_ARG; }
@@ -397,6 +423,7 @@ svdq_status_t pack_on_host(const svdq_pack_params_t* p, HostPack* out, std::stri
 #pragma omp parallel for schedule(static)
     for (int64_t n = 0; n < N; ++n)
       quantize_row(R.data() + n * K, K, o.s_gW, o.R_codes.data() + n * K / 2, o.R_scales.data() + n * K / 16);
+    if (R_keep) R_keep->swap(R);
     // activation global scale
     if (p->Xcal_bf16) {
       float xa = 0.f;

@@ -29,7 +29,9 @@ struct HostPack {
 };
 
 // Validates p and runs smoothing, SVD, residual and NVFP4 quantisation on the CPU.
-svdq_status_t pack_on_host(const svdq_pack_params_t* p, HostPack* out, std::string* err);
+// R_keep, when non-null, receives the float32 residual R (N x K) that was quantised.
+svdq_status_t pack_on_host(const svdq_pack_params_t* p, HostPack* out, std::string* err,
+                           std::vector<float>* R_keep = nullptr);
 
 // AWQ-style W4A16 layer: host pack (awq_host.cpp) and GEMV (awq_gemv.cu).
 struct AwqHostPack {
@@ -129,7 +131,45 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 int k2_launch(const K2Maps& maps, const K2Args& a, int sm_count, void* stream);
 size_t k2_smem_bytes();
 
+// ------------------------------------------------------------------ INT4 variant (int4_path.cu)
+// Symmetric INT4 groups: nibble q + 8, q in [-7, 7], one float32 scale per 64 elements along K.
+// Activation and weight group scales are stored group-major, [K / 64][rows padded to 128].
+void int4_quantize_row(const float* v, int64_t K, uint8_t* codes, float* scales);   // host (pack_host.cpp)
+struct alignas(64) Int4K1Maps {
+  unsigned char X[128];     // CUtensorMap: X        (bf16, K x M, box 64 x 32, swizzle 128)
+  unsigned char L1t[128];   // CUtensorMap: L1'^T    (bf16, K x r_pad, box 64 x r_pad, swizzle 128)
+};
+struct Int4K1Args {
+  const float* inv_lambda;  // K
+  uint8_t* codes;           // M x K/2
+  float* scales;            // [K/64][scale_ld]
+  uint16_t* T;              // M x r_pad bf16, T = X^ L1 (unscaled)
+  int64_t M, K, scale_ld;
+  int r_pad;
+  int* err;                 // device error word
+  uint64_t wait_ns;
+};
+struct alignas(64) Int4K2Maps {
+  unsigned char A[128];     // CUtensorMap: x codes  (u8, K/2 x M, box 32 x 128)
+  unsigned char B[128];     // CUtensorMap: R codes  (u8, K/2 x N, box 32 x 128)
+  unsigned char SA[128];    // CUtensorMap: x scales (f32, M_pad x K/64, box 128 x 1)
+  unsigned char SB[128];    // CUtensorMap: R scales (f32, N_pad x K/64, box 128 x 1)
+  unsigned char T[128];     // CUtensorMap: T        (bf16, r_pad x M, box 64 x 128, swizzle 128)
+  unsigned char L2[128];    // CUtensorMap: L2^T     (bf16, r_pad x N, box 64 x 128, swizzle 128)
+};
+struct Int4K2Args {
+  const uint16_t* bias;     // N bf16
+  uint16_t* Y;              // M x N bf16
+  int64_t M, N, K;
+  int r_pad;
+  int* err;
+  uint64_t wait_ns;
+};
+int int4_k1_launch(const Int4K1Maps& maps, const Int4K1Args& a, void* stream);
+int int4_k2_launch(const Int4K2Maps& maps, const Int4K2Args& a, void* stream);
+
 // Tensor-map encoding through the driver entry point (api.cu).
+// dtype_bytes: 1 (u8), 2 (bf16) or 4 (f32)
 bool encode_map_2d(void* map, int dtype_bytes, const void* base, uint64_t inner, uint64_t outer,
                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle128,
                    std::string* err);

@@ -66,6 +66,13 @@ class AwqHost(ctypes.Structure):
     ]
 
 
+class Int4Host(ctypes.Structure):
+    _fields_ = [
+        ("lam", _vp), ("inv_lambda", _vp), ("L1_bf16", _vp), ("L2_bf16", _vp), ("R_codes", _vp),
+        ("R_scales", _vp), ("bias_bf16", _vp),
+    ]
+
+
 _SIGS = {
     "svdq_pack_host": (_i32, [ctypes.POINTER(PackParams), ctypes.POINTER(PackedHost)]),
     "svdq_pack_weights": (_i32, [ctypes.POINTER(PackParams), ctypes.POINTER(_vp)]),
@@ -91,6 +98,15 @@ _SIGS = {
     "svdq_awq_export": (_i32, [_vp, ctypes.POINTER(AwqHost)]),
     "svdq_awq_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_awq_check_error": (_i32, [_vp]),
+    "svdq_int4_scale_ld": (_i64, [_i64]),
+    "svdq_int4_pack_host": (_i32, [ctypes.POINTER(PackParams), ctypes.POINTER(Int4Host)]),
+    "svdq_int4_pack": (_i32, [ctypes.POINTER(PackParams), ctypes.POINTER(_vp)]),
+    "svdq_int4_export": (_i32, [_vp, ctypes.POINTER(Int4Host)]),
+    "svdq_int4_reserve": (_i32, [_vp, _i64]),
+    "svdq_int4_quantize_act": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "svdq_int4_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
+    "svdq_int4_check_error": (_i32, [_vp]),
+    "svdq_int4_destroy": (_i32, [_vp]),
     "svdq_status_string": (ctypes.c_char_p, [_i32]),
     "svdq_last_error": (ctypes.c_char_p, []),
 }
@@ -305,6 +321,71 @@ class Layer:
             raise ValueError(f"LoRA factors must be {self.K} x r and r x {self.N}")
         check(LIB.svdq_attach_lora(self.h, A.ctypes.data, B.ctypes.data, r_lora, float(scale), _stream(stream)),
               "svdq_attach_lora")
+
+
+# ------------------------------------------------------------------ INT4 variant
+def _int4_out(N, K, rank):
+    o = dict(lam=np.zeros(K, np.float32), inv_lambda=np.zeros(K, np.float32),
+             L1=np.zeros((K, rank), np.uint16), L2=np.zeros((rank, N), np.uint16),
+             R_codes=np.zeros((N, K // 2), np.uint8), R_scales=np.zeros((N, K // 64), np.float32),
+             bias=np.zeros(N, np.uint16), rank=rank, fmt="int4")
+    st = Int4Host(lam=_ptr(o["lam"]), inv_lambda=_ptr(o["inv_lambda"]), L1_bf16=_ptr(o["L1"]),
+                  L2_bf16=_ptr(o["L2"]), R_codes=_ptr(o["R_codes"]), R_scales=_ptr(o["R_scales"]),
+                  bias_bf16=_ptr(o["bias"]))
+    return o, st
+
+
+def int4_pack_host(W, rank, **kw):
+    """svdq_int4_pack_host: the INT4 variant's offline step on the CPU (codes two per byte)."""
+    p, keep = make_params(W, rank, **kw)
+    o, st = _int4_out(int(p.N), int(p.K), rank)
+    check(LIB.svdq_int4_pack_host(ctypes.byref(p), ctypes.byref(st)), "svdq_int4_pack_host")
+    return o
+
+
+def int4_scale_ld(rows: int) -> int:
+    return int(LIB.svdq_int4_scale_ld(rows))
+
+
+class Int4Layer:
+    """A packed INT4-variant SVDQuant layer on one CUDA device (wraps an svdq_int4_handle_t)."""
+
+    def __init__(self, W, rank, **kw):
+        p, keep = make_params(W, rank, **kw)
+        h = _vp()
+        check(LIB.svdq_int4_pack(ctypes.byref(p), ctypes.byref(h)), "svdq_int4_pack")
+        self.h = h
+        self.N, self.K, self.rank = int(p.N), int(p.K), int(rank)
+        self.r_pad = 0 if rank == 0 else 64 * ((rank + 63) // 64)
+
+    def close(self):
+        if getattr(self, "h", None):
+            LIB.svdq_int4_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def export(self):
+        o, st = _int4_out(self.N, self.K, self.rank)
+        check(LIB.svdq_int4_export(self.h, ctypes.byref(st)), "svdq_int4_export")
+        return o
+
+    def reserve(self, M_max: int):
+        check(LIB.svdq_int4_reserve(self.h, M_max), "svdq_int4_reserve")
+
+    def quantize_act(self, X, M, codes, scales, T=None, stream=None):
+        check(LIB.svdq_int4_quantize_act(self.h, _ptr(X), M, _ptr(codes), _ptr(scales), _ptr(T), _stream(stream)),
+              "svdq_int4_quantize_act")
+
+    def forward(self, X, Y, M, stream=None):
+        check(LIB.svdq_int4_forward(self.h, _ptr(X), _ptr(Y), M, _stream(stream)), "svdq_int4_forward")
+
+    def check_error(self):
+        check(LIB.svdq_int4_check_error(self.h), "svdq_int4_check_error")
 
 
 # ------------------------------------------------------------------ AWQ-style W4A16 layer
