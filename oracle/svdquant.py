@@ -35,6 +35,8 @@ Eckart-Young (residual energy equals the tail of the spectrum computed through
 an eigen-decomposition); full rank leaves R = 0; lambda = 1 with r = 0 equals
 plain W4A4 quantisation of X and W; a pure-Python loop evaluation of the
 forward on 4 x 16 x 16; SVDQuant beats naive W4A4 on outlier-heavy inputs.
+The MLP pair (gelu, mlp_down_input, mlp_pair_forward) composes two layers through the
+activation; gelu is pinned to hand values of y * Phi(y) and its limits.
 The INT4 variant (pack_int4, quantize_act_int4, forward_int4) shares every step up to the
 residual and quantises with oracle.int4 instead; its pins mirror the NVFP4 ones (reduction to
 plain INT4 W4A4 at lambda = 1 and r = 0, loops on a tiny case, the method claim on outliers).
@@ -222,6 +224,34 @@ def lora_delta(X_bits, A_bits, B_bits, scale, rows=None):
     if rows is not None:
         Xb = Xb[rows]
     return float(scale) * ((bf16_to_f64(Xb) @ bf16_to_f64(A_bits)) @ bf16_to_f64(B_bits))
+
+
+# ----------------------------------------------------------------------------- MLP pair
+def gelu(y) -> np.ndarray:
+    """GELU(y) = y * Phi(y) = 0.5 * y * (1 + erf(y / sqrt(2))) in float64 (the erf form; the pages
+    name the MLP's activation without a formula)."""
+    from math import erf, sqrt
+    y = np.asarray(y, np.float64)
+    return 0.5 * y * (1.0 + np.vectorize(erf)(y / sqrt(2.0)))
+
+
+def mlp_down_input(Y_up_bits, p_down):
+    """What the MLP-down layer receives from MLP-up in an MLP pair: G = bf16(GELU(Y_up)) with Y_up
+    the up layer's bf16 output, then the down layer's run-time quantisation of G (smoothing by its
+    inv_lambda, NVFP4 blocks with its s_gX) and its down-projection T = G^ L1_down (float64).
+    Returns (G bits, codes, scales, x^ float32, T)."""
+    G = f64_to_bf16(gelu(bf16_to_f64(Y_up_bits)))
+    codes, scales, xh = quantize_act(G, p_down["inv_lambda"], p_down["s_gX"])
+    T = lowrank_down(xh, p_down["L1"]) if p_down["rank"] else np.zeros((G.shape[0], 0))
+    return G, codes, scales, xh, T
+
+
+def mlp_pair_forward(X_bits, p_up, p_down):
+    """The MLP pair: Y_up = forward(X, up) rounded to bf16, G = bf16(GELU(Y_up)), Y = forward(G, down)
+    in float64."""
+    Y_up = f64_to_bf16(forward(X_bits, p_up))
+    G = f64_to_bf16(gelu(bf16_to_f64(Y_up)))
+    return forward(G, p_down)
 
 
 # ----------------------------------------------------------------------------- references

@@ -272,3 +272,35 @@ def test_int4_svdquant_beats_naive_int4_on_outliers(name):
     e_svdq = sq.rel_fro(sq.forward_int4(d["X"], p), ref)
     e_naive = sq.rel_fro(_naive_int4(d["X"], d["W"], d["bias"]), ref)
     assert e_svdq < e_naive, (e_svdq, e_naive)
+
+
+# ----------------------------------------------------------------------------- MLP pair
+def test_gelu_hand_values_and_limits():
+    """GELU(y) = y Phi(y): Phi(1) = 0.8413447460685429, Phi(-1) = 0.15865525393145707,
+    Phi(2) = 0.9772498680518208 (standard normal table values); 0 at 0; y for large y; 0 for very
+    negative y; odd part y/2 (GELU(y) - GELU(-y) = y)."""
+    g = sq.gelu(np.array([0.0, 1.0, -1.0, 2.0, 40.0, -40.0, 0.5, -0.5]))
+    assert g[0] == 0.0
+    assert abs(g[1] - 0.8413447460685429) < 1e-15 and abs(g[2] + 0.15865525393145707) < 1e-15
+    assert abs(g[3] - 2 * 0.9772498680518208) < 1e-15
+    assert g[4] == 40.0 and abs(g[5]) < 1e-300
+    assert abs((g[6] - g[7]) - 0.5) < 1e-15
+
+
+def test_mlp_pair_is_the_composition_of_the_pinned_steps(tiny):
+    """The pair's forward equals the down layer's forward on bf16(GELU(bf16(up forward))); the down
+    input's codes are the down layer's quantiser applied to that G; T = x^ L1."""
+    w, d = tiny
+    up = sq.pack(d["W"], d["bias"], w.rank, Xcal_bits=d["X"])
+    rng = np.random.default_rng(3)
+    Wd = synthetic.f64_to_bf16_bits(rng.standard_normal((64, w.N)) / np.sqrt(w.N))
+    Yup = sq.f64_to_bf16(sq.forward(d["X"], up))
+    Gref = sq.f64_to_bf16(sq.gelu(sq.bf16_to_f64(Yup)))
+    down = sq.pack(Wd, None, 16, Xcal_bits=Gref)
+    G, c, s, xh, T = sq.mlp_down_input(Yup, down)
+    assert np.array_equal(G, Gref)
+    c2, s2, xh2 = sq.quantize_act(Gref, down["inv_lambda"], down["s_gX"])
+    assert np.array_equal(c, c2) and np.array_equal(s, s2)
+    assert np.allclose(T, xh2.astype(np.float64) @ sq.bf16_to_f64(down["L1"]), rtol=1e-12, atol=0)
+    Y = sq.mlp_pair_forward(d["X"], up, down)
+    assert np.array_equal(Y, sq.forward(Gref, down))
