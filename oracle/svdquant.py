@@ -228,11 +228,13 @@ def lora_delta(X_bits, A_bits, B_bits, scale, rows=None):
 
 # ----------------------------------------------------------------------------- MLP pair
 def gelu(y) -> np.ndarray:
-    """GELU(y) = y * Phi(y) = 0.5 * y * (1 + erf(y / sqrt(2))) in float64 (the erf form; the pages
-    name the MLP's activation without a formula)."""
-    from math import erf, sqrt
+    """GELU(y) = y * Phi(y), Phi the standard normal CDF, in float64 (the pages name the MLP's
+    activation without a formula; this is GELU's definition, not the tanh approximation).
+    Phi(y) = erfc(-y / sqrt(2)) / 2 (scipy.special.erfc): the same function as (1 + erf(y/sqrt(2)))/2,
+    but without the cancellation that rounds Phi to 0 for y below about -8.3."""
+    from scipy.special import erfc
     y = np.asarray(y, np.float64)
-    return 0.5 * y * (1.0 + np.vectorize(erf)(y / sqrt(2.0)))
+    return y * (0.5 * erfc(-y / np.sqrt(2.0)))
 
 
 def mlp_down_input(Y_up_bits, p_down):

@@ -277,14 +277,16 @@ def test_int4_svdquant_beats_naive_int4_on_outliers(name):
 # ----------------------------------------------------------------------------- MLP pair
 def test_gelu_hand_values_and_limits():
     """GELU(y) = y Phi(y): Phi(1) = 0.8413447460685429, Phi(-1) = 0.15865525393145707,
-    Phi(2) = 0.9772498680518208 (standard normal table values); 0 at 0; y for large y; 0 for very
-    negative y; odd part y/2 (GELU(y) - GELU(-y) = y)."""
-    g = sq.gelu(np.array([0.0, 1.0, -1.0, 2.0, 40.0, -40.0, 0.5, -0.5]))
+    Phi(2) = 0.9772498680518208, Phi(-10) = 7.619853024160527e-24 (standard normal tail value);
+    0 at 0; y for large y; odd part y/2 (GELU(y) - GELU(-y) = y).  The Phi(-10) pin fails for the
+    1 + erf form, which cancels to 0 there."""
+    g = sq.gelu(np.array([0.0, 1.0, -1.0, 2.0, 40.0, -40.0, 0.5, -0.5, -10.0]))
     assert g[0] == 0.0
     assert abs(g[1] - 0.8413447460685429) < 1e-15 and abs(g[2] + 0.15865525393145707) < 1e-15
     assert abs(g[3] - 2 * 0.9772498680518208) < 1e-15
-    assert g[4] == 40.0 and abs(g[5]) < 1e-300
+    assert g[4] == 40.0 and g[5] <= 0.0 and abs(g[5]) < 1e-300
     assert abs((g[6] - g[7]) - 0.5) < 1e-15
+    assert abs(g[8] / (-10.0 * 7.619853024160527e-24) - 1.0) < 1e-12
 
 
 def test_mlp_pair_is_the_composition_of_the_pinned_steps(tiny):
