@@ -450,6 +450,86 @@ def measure_int4(torch, svdq, w, pt, stream, flush, bf16_peak, reps=50, warm=5):
     return out
 
 
+def measure_mlp_pair(torch, svdq, pw, stream, flush, reps=50, warm=5):
+    """The MLP pair (up layer, GELU, down layer) run unfused (svdq_linear_forward, svdq_gelu_bf16,
+    svdq_linear_forward) and fused (svdq_mlp_forward: the up layer's kernel 2 writes the down
+    layer's quantised input); medians with cold and warm L2, and the parts of each."""
+    up_w, dn_w = pw.up, pw.down
+    M, K, Nu, N = up_w.M, up_w.K, up_w.N, dn_w.N
+    d = synthetic.make(up_w)
+    up = svdq.Layer(d["W"], up_w.rank, bias=d["bias"], Xcal=d["X"], M_max=M)
+    X = torch.from_numpy(d["X"].view(np.int16)).cuda()
+    Yup = torch.empty((M, Nu), dtype=torch.bfloat16, device="cuda")
+    G = torch.empty_like(Yup)
+    up.forward(X, Yup, M, stream)
+    svdq.gelu_bf16(Yup, G, M * Nu, stream)
+    torch.cuda.synchronize()
+    # the down layer calibrated on its real input (a sample of rows of G)
+    Gcal = G[: min(M, 1024)].view(torch.int16).cpu().numpy().view(np.uint16)
+    wd = synthetic.make_weights(dn_w)
+    down = svdq.Layer(wd["W"], dn_w.rank, bias=wd["bias"], Xcal=Gcal, M_max=M)
+    mlp = svdq.Mlp(up, down, M)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    codes = torch.empty((M, Nu // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(svdq.scales_bytes(M, Nu), dtype=torch.uint8, device="cuda")
+    T = torch.empty((M, max(down.info.r_pad, 8)), dtype=torch.int16, device="cuda")
+
+    def unfused(i, ev):
+        if ev:
+            ev[0].record(stream)
+        up.forward(X, Yup, M, stream)
+        if ev:
+            ev[1].record(stream)
+        svdq.gelu_bf16(Yup, G, M * Nu, stream)
+        if ev:
+            ev[2].record(stream)
+        down.forward(G, Y, M, stream)
+        if ev:
+            ev[3].record(stream)
+
+    def fused(i, ev):
+        if ev:
+            ev[0].record(stream)
+        mlp.up_quantize(X, M, codes, scales, T, stream)
+        if ev:
+            ev[1].record(stream)
+        down.gemm_quantized(codes, scales, T, Y, M, stream)
+        if ev:
+            ev[2].record(stream)
+
+    def whole(i, ev):
+        if ev:
+            ev[0].record(stream)
+        mlp.forward(X, Y, M, stream)
+        if ev:
+            ev[1].record(stream)
+
+    med = lambda rows, j: round(1e3 * statistics.median(r[j] for r in rows), 2)
+    out = {}
+    for mode, fl in (("cold_l2", flush), ("warm_l2", None)):
+        u = time_events(torch, stream, unfused, reps, warm, fl, 4)
+        f = time_events(torch, stream, fused, reps, warm, fl, 3)
+        h = time_events(torch, stream, whole, reps, warm, fl, 2)
+        out[mode] = {"unfused_us": round(1e3 * statistics.median(sum(r) for r in u), 2),
+                     "unfused_up_us": med(u, 0), "unfused_gelu_us": med(u, 1), "unfused_down_us": med(u, 2),
+                     "fused_us": med(h, 0), "fused_up_quantize_us": med(f, 0), "fused_down_gemm_us": med(f, 1)}
+    mlp.check_error()
+    flops = 2.0 * M * Nu * K + 2.0 * M * N * Nu + 2.0 * M * up_w.rank * (K + Nu) + 2.0 * M * dn_w.rank * (Nu + N)
+    c = out["cold_l2"]
+    out.update(workload=pw.name, M=M, K=K, N_up=Nu, N=N, ranks=[up_w.rank, dn_w.rank],
+               tflops_fused=flops / (c["fused_us"] * 1e-6) / 1e12,
+               tflops_unfused=flops / (c["unfused_us"] * 1e-6) / 1e12,
+               speedup=c["unfused_us"] / c["fused_us"],
+               hbm_bytes_avoided=4 * M * Nu * 2,
+               note="unfused = up forward, GELU kernel, down forward; fused = up kernels 1 and 2 with the "
+                    "GELU + next-layer quantiser epilogue and the T reduction, then the down layer's kernel 2; "
+                    "avoided: Y_up written, GELU's read and write, the down kernel 1's read of G")
+    mlp.close()
+    down.close()
+    up.close()
+    return out
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -525,6 +605,8 @@ def run_ours(args, w):
     int4 = None
     if world == 1 and not args.no_sweep:
         int4 = measure_int4(torch, svdq, w, pt, stream, flush, bf16)
+        sweep[synthetic.MLP_PAIR.name] = measure_mlp_pair(torch, svdq, synthetic.MLP_PAIR, stream, flush)
+        torch.cuda.empty_cache()
         for sw in synthetic.SWEEP:
             if sw.name == w.name:
                 sweep[sw.name] = point_summary(sw, t, hbm, fp4_peak)

@@ -289,6 +289,71 @@ const char* svdq_status_string(svdq_status_t s);
 const char* svdq_last_error(void);
 
 /* ==================================================================================
+ * MLP pair: two SVDQuant layers with GELU between them, the up layer's output feeding the down
+ * layer (the FLUX transformer block's feed-forward: K -> N_up -> N).
+ *
+ * The pages' Nunchaku section says the low-rank and 4-bit branches run as one fused operation
+ * that shares inputs and outputs so that memory-bound diffusion transformers avoid redundant
+ * memory traffic (aiflownews article on Nunchaku in Diffusers, "Nunchaku: the inference engine
+ * that makes SVDQuant practical").  The pair carries that sharing across the activation: the up
+ * layer's kernel 2 applies GELU to its bf16 output tile and writes the down layer's kernel-1
+ * outputs for it (NVFP4 codes, E4M3 block scales and the low-rank down-projection T), so the
+ * up layer's output is never written to memory and the down layer's kernel 1 never runs.
+ *
+ * Arithmetic (identical to running the layers apart with svdq_gelu_bf16 between them, except
+ * for the float32 summation order of T):
+ *   Y_up = bf16(alpha_up * acc + b_up)              the up layer's output, bit for bit
+ *   G    = bf16(GELU(Y_up)),  GELU(y) = y * Phi(y), Phi the standard normal CDF (the pages
+ *          name no activation formula: this is GELU's definition, not the tanh approximation),
+ *          evaluated in float32 as y Q(|y|) (y <= 0) or y (1 - Q(y)) with the normal tail
+ *          Q(u) = erfc(u / sqrt(2)) / 2 from the Chebyshev fit of erfc in Numerical Recipes
+ *          (section 6.2, erfcc); relative error below 2^-19 (y >= 0), 2^-19 + y^2 2^-22 (y < 0)
+ *   codes, scales of G: the down layer's smoothing and NVFP4 quantiser (as svdq_quantize_act)
+ *   T    = bf16(fl32(sum of partial G L1') * fl32(1 / alpha_down)), L1' = diag(1/lambda) L1 in
+ *          bf16 as kernel 1 uses it; the partial sums (float32, one per run of column tiles and
+ *          half tile) are added in a fixed order, so T is reproducible from run to run.
+ * Limits: the up layer's N equals the down layer's K; the down layer's kernel rank (SVD rank
+ * plus any LoRA rank) is at most 64.  The pair keeps the down layer's L1' in the order the
+ * epilogue reads it; attaching LoRA factors to the down layer afterwards invalidates the pair
+ * (its calls then return SVDQ_ERR_INVALID_ARG).  Both handles must outlive the pair.
+ * Errors: the fused kernel reports bounded-wait expiry on the up handle's error word, the down
+ * layer's kernel 2 on the down handle's; svdq_mlp_check_error reads both.
+ * ================================================================================== */
+typedef struct svdq_mlp* svdq_mlp_t;
+
+/* svdq_mlp_create -- binds two packed layers (up: N_up x K, down: N x N_up) on one device and
+ * allocates the pair's buffers for up to M_max rows: the down layer's L1' in fragment order
+ * (N_up x rank bf16) and the partial sums of T (at most about 2 * N_up/256 * M_max * rank * 4
+ * bytes, far less at large M).  Errors: SVDQ_ERR_INVALID_ARG (null, same handle twice, other
+ * devices, N_up != K_down), SVDQ_ERR_UNSUPPORTED_SHAPE (down rank > 64), SVDQ_ERR_OOM. */
+svdq_status_t svdq_mlp_create(svdq_handle_t up, svdq_handle_t down, int64_t M_max, svdq_mlp_t* out);
+svdq_status_t svdq_mlp_destroy(svdq_mlp_t p);
+
+/* svdq_mlp_up_quantize -- the up layer's kernel 1 on X (device M x K bf16), then its kernel 2
+ * with the fused epilogue and the reduction of T: writes the down layer's kernel-1 outputs for
+ * G = bf16(GELU(Y_up)) into x_codes (M x N_up/2), x_scales (tiled, svdq_scales_bytes(M, N_up))
+ * and T (M x r_pad_down bf16; may be NULL when the down rank is 0), exactly the buffers
+ * svdq_gemm_quantized of the down layer consumes.  Uses the up layer's workspace
+ * (svdq_reserve(up, >= M)).  M <= M_max.  Outputs must not overlap X or each other. */
+svdq_status_t svdq_mlp_up_quantize(svdq_mlp_t p, const void* X_bf16, int64_t M, void* x_codes,
+                                   void* x_scales, void* T_bf16, void* stream);
+
+/* svdq_mlp_forward -- the whole pair on `stream`: svdq_mlp_up_quantize into the down layer's
+ * workspace, then the down layer's kernel 2.  X: device M x K bf16; Y: device M x N bf16
+ * (written once).  Needs both layers' workspaces for M (svdq_reserve) and M <= M_max.  X and Y
+ * must not overlap each other or either workspace's kernel scratch. */
+svdq_status_t svdq_mlp_forward(svdq_mlp_t p, const void* X_bf16, void* Y_bf16, int64_t M, void* stream);
+
+/* svdq_mlp_check_error -- svdq_check_error of the up layer, then of the down layer (both are
+ * read and cleared); returns the first failure. */
+svdq_status_t svdq_mlp_check_error(svdq_mlp_t p);
+
+/* svdq_gelu_bf16 -- G[i] = bf16(GELU(Y[i])) for n bf16 values (n % 8 == 0, 16-byte aligned
+ * device buffers, G == Y allowed), with the fused epilogue's arithmetic: the unfused pair is
+ * svdq_linear_forward(up), this, svdq_linear_forward(down).  Runs on the current device. */
+svdq_status_t svdq_gelu_bf16(const void* Y_bf16, void* G_bf16, int64_t n, void* stream);
+
+/* ==================================================================================
  * INT4 variant of the SVDQuant layer
  *
  * The pages say SVDQuant supports both INT4 and FP4 and that Nunchaku runs INT4 kernels on

@@ -26,7 +26,7 @@ CXX_FLAGS = ["-O3", "-std=c++17", "-fPIC", "-fopenmp", "-ffp-contract=off", "-I"
 
 CU_SOURCES = ["api.cu", "k1_actquant.cu", "k2_fp4gemm.cu", "awq_gemv.cu", "int4_path.cu", "int4_api.cu"]
 CXX_SOURCES = ["pack_host.cpp", "awq_host.cpp"]
-HEADERS = ["svdq_internal.h", "ptx.cuh", "abi_util.cuh"]
+HEADERS = ["svdq_internal.h", "ptx.cuh", "abi_util.cuh", "nvfp4_block.cuh"]
 
 
 def _nvcc() -> str:

@@ -120,6 +120,7 @@ struct svdq_layer {
   // which kernel's MMA warp waits on a barrier nothing completes (0 none, 1 kernel 1, 2 kernel 2)
   uint64_t wait_ns = kDefaultWaitNs;
   int stall = 0;
+  uint64_t low_rank_gen = 0;       // counts uploads of the low-rank factors (MLP pairs check it)
 };
 
 namespace {
@@ -184,6 +185,15 @@ void free_layer(svdq_layer* h) {
 //        L1' = diag(1/lambda) L1 for the SVD columns (kernel 1 multiplies raw X by it, which
 //        is X^ L1), and bf16(scale * A) for the LoRA columns (X A needs no smoothing)
 //   L2t  N x r_pad bf16: L2 transposed, then B transposed, zero padding
+// Column j of L1' at row k (bf16 bits): bf16(1/lambda_k * L1[k][j]) for an SVD column, the
+// scaled LoRA A for a LoRA column.
+uint16_t l1_prime(const svdq_layer* h, int64_t k, int64_t j) {
+  const HostPack& hp = h->host;
+  const int64_t r = hp.rank;
+  return j < r ? f64_to_bf16(double(hp.inv_lambda[k]) * double(bf16_to_f32(hp.L1[k * r + j])))
+               : h->lora_A[k * h->r_lora + (j - r)];
+}
+
 svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
   const HostPack& hp = h->host;
   const int64_t N = hp.N, K = hp.K, r = hp.rank, rl = h->r_lora, rk = r + rl;
@@ -204,8 +214,7 @@ svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
     for (int64_t j = 0; j < rk; ++j)
       for (int i = 0; i < 64; ++i) {
         const int64_t k = 64 * c + i;
-        const uint16_t v = j < r ? f64_to_bf16(double(hp.inv_lambda[k]) * double(bf16_to_f32(hp.L1[k * r + j])))
-                                 : h->lora_A[k * rl + (j - r)];
+        const uint16_t v = l1_prime(h, k, j);
         const int unit = (i / 8) ^ int(j % 8);
         reinterpret_cast<uint16_t*>(slice + j * 128 + unit * 16)[i % 8] = v;
       }
@@ -243,6 +252,7 @@ svdq_status_t upload_low_rank(svdq_layer* h, cudaStream_t stream) {
   h->d_LI = d_li;
   h->maps = maps;
   h->r_pad = r_pad;
+  ++h->low_rank_gen;
   return SVDQ_OK;
 }
 
@@ -805,6 +815,223 @@ extern "C" svdq_status_t svdq_linear_forward_noalloc(svdq_handle_t h, const void
   if (e1 != 0) return cuda_fail(cudaError_t(e1), "kernel 1 launch");
   return launch_k2(h, a.x_codes, a.x_scales, a.T, Y, M, s);
 }
+
+// ------------------------------------------------------------------ MLP pair (fused epilogue)
+// The up layer's kernel 2 writes the down layer's kernel-1 outputs for G = bf16(GELU(Y_up))
+// (codes, scales and partial sums of G L1'), so Y_up is never written to memory and the down
+// layer's kernel 1 does not run.  The pair owns the down layer's L1' in warp-MMA fragment order
+// and the partial sums; the activations pass through the two layers' workspaces.
+struct svdq_mlp {
+  svdq_layer* up = nullptr;
+  svdq_layer* down = nullptr;
+  int device = 0;
+  int rd = 0;                       // the down layer's kernel rank
+  uint64_t down_gen = 0;            // its low-rank upload the fragments were built from
+  int pairs = 0;                    // CTA pairs of the fused kernel on this device
+  int64_t M_max = 0;
+  uint16_t* d_l1f = nullptr;        // N_up x rd bf16 in fragment order
+  float* d_part = nullptr;          // partial sums
+  size_t part_bytes = 0;
+};
+
+namespace {
+
+// Bytes of partial sums the fused epilogue writes for M rows.
+size_t mlp_part_bytes(const svdq_mlp* p, int64_t M) {
+  if (p->rd == 0 || M == 0) return 0;
+  const int64_t N = p->up->host.N;
+  const int U = k2_fused_unit_len(M, N, p->pairs);
+  return size_t(k2_fused_partials(M, N, U)) * size_t(M) * size_t(p->rd) * 4;
+}
+
+void free_mlp(svdq_mlp* p) {
+  cudaFree(p->d_l1f);
+  cudaFree(p->d_part);
+}
+
+// Kernel 1 of the up layer on X, then its kernel 2 with the fused epilogue writing the down
+// layer's codes, scales and T (through the partial sums and their reduction).
+svdq_status_t mlp_up(svdq_mlp* p, const void* X, int64_t M, void* codes, void* scales, void* T, cudaStream_t stream) {
+  svdq_layer* up = p->up;
+  svdq_layer* dn = p->down;
+  const WsLayout w = ws_layout(up, up->ws_M, up->ws_staging);
+  void* ucodes = up->ws + w.codes;
+  void* uscales = up->ws + w.scales;
+  void* uT = up->rank_k() ? up->ws + w.T : nullptr;
+  svdq_status_t st = launch_k1(up, X, M, ucodes, uscales, uT, stream);
+  if (st != SVDQ_OK) return st;
+  const int64_t K = up->host.K, N = up->host.N;
+  K2Maps maps = up->maps;
+  std::string err;
+  if (!encode_map_2d(maps.A, 1, ucodes, K / 2, M, K / 2, 128, 128, 1, &err) ||
+      !encode_map_2d(maps.SFA, 1, uscales, 256, svdq_scales_bytes(M, K) / 256, 256, 256, 8, 0, &err))
+    return fail(SVDQ_ERR_CUDA, err);
+  if (up->rank_k() > 0 && !encode_map_2d(maps.T, 2, uT, up->r_pad, M, up->r_pad * 2, 64, 128, 1, &err))
+    return fail(SVDQ_ERR_CUDA, err);
+  K2Args a{};
+  a.bias = up->d_bias;
+  a.err = up->d_err;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.rank = int(up->rank_k());
+  a.alpha = up->host.alpha;
+  a.wait_ns = up->wait_ns;
+  a.stall = up->stall == 2;
+  a.unit_len = k2_fused_unit_len(M, N, p->pairs);
+  a.fuse.inv_lambda = dn->d_inv_lambda;
+  a.fuse.qtab = dn->d_qtab;
+  a.fuse.inv_six = dn->inv_six;
+  a.fuse.x_codes = static_cast<uint8_t*>(codes);
+  a.fuse.x_scales = static_cast<uint8_t*>(scales);
+  a.fuse.l1f = p->d_l1f;
+  a.fuse.part = p->d_part;
+  a.fuse.rd = p->rd;
+  int e = k2_fused_launch(maps, a, up->sm_count, stream);
+  if (e != 0) return cuda_fail(cudaError_t(e), "fused kernel 2 launch");
+  if (p->rd > 0) {
+    e = k2_t_reduce_launch(p->d_part, k2_fused_partials(M, N, a.unit_len), M, p->rd, int(dn->r_pad), dn->inv_alpha,
+                           static_cast<uint16_t*>(T), stream);
+    if (e != 0) return cuda_fail(cudaError_t(e), "partial-sum reduction launch");
+  }
+  return SVDQ_OK;
+}
+
+svdq_status_t mlp_check(const svdq_mlp* p, int64_t M) {
+  if (p->down->low_rank_gen != p->down_gen)
+    return fail(SVDQ_ERR_INVALID_ARG, "the down layer's low-rank factors changed after svdq_mlp_create");
+  if (p->up->host.N != p->down->host.K) return fail(SVDQ_ERR_INVALID_ARG, "layer shapes changed");
+  if (M > p->M_max) return fail(SVDQ_ERR_WORKSPACE, "M is larger than the pair's M_max");
+  if (!p->up->ws || p->up->ws_M < M) return fail(SVDQ_ERR_WORKSPACE, "no up-layer workspace for this M (svdq_reserve)");
+  return SVDQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+svdq_status_t svdq_mlp_create(svdq_handle_t up, svdq_handle_t down, int64_t M_max, svdq_mlp_t* out) {
+  if (!up || !down || !out || M_max < 0) return fail(SVDQ_ERR_INVALID_ARG, "null argument or negative M_max");
+  if (up == down) return fail(SVDQ_ERR_INVALID_ARG, "the up and down layers must be different handles");
+  if (up->device != down->device) return fail(SVDQ_ERR_INVALID_ARG, "the layers live on different devices");
+  if (up->host.N != down->host.K)
+    return fail(SVDQ_ERR_INVALID_ARG, "the up layer's N must equal the down layer's K");
+  const int64_t rd = down->rank_k();
+  if (rd > kFuseMaxRank)
+    return fail(SVDQ_ERR_UNSUPPORTED_SHAPE, "the fused epilogue supports a down-layer rank (with LoRA) of at most 64");
+  svdq_mlp* p = new (std::nothrow) svdq_mlp();
+  if (!p) return fail(SVDQ_ERR_OOM, "host allocation failed");
+  DeviceGuard guard(up->device);
+  p->up = up;
+  p->down = down;
+  p->device = up->device;
+  p->rd = int(rd);
+  p->down_gen = down->low_rank_gen;
+  p->pairs = k2_fused_pairs(up->sm_count);
+  p->M_max = M_max;
+  const int64_t N = up->host.N;
+  // the largest partial-sum buffer any M <= M_max needs (the schedule depends on M's row blocks)
+  size_t part = 0;
+  for (int64_t mb = 1; mb <= ceil_div(M_max, 256); ++mb)
+    part = std::max(part, mlp_part_bytes(p, std::min<int64_t>(mb * 256, M_max)));
+  cudaError_t e = cudaSuccess;
+  if (rd > 0) {
+    std::vector<uint16_t> l1(size_t(N) * rd), frag(size_t(N) * rd);
+    for (int64_t k = 0; k < N; ++k)
+      for (int64_t j = 0; j < rd; ++j) l1[k * rd + j] = l1_prime(down, k, j);
+    k2_l1_fragments(l1.data(), N, int(rd), frag.data());
+    p->d_l1f = static_cast<uint16_t*>(dalloc(frag.size() * 2, &e));
+    if (e == cudaSuccess) e = cudaMemcpy(p->d_l1f, frag.data(), frag.size() * 2, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && part) p->d_part = static_cast<float*>(dalloc(part, &e));
+  }
+  if (e != cudaSuccess) {
+    free_mlp(p);
+    delete p;
+    return e == cudaErrorMemoryAllocation ? fail(SVDQ_ERR_OOM, "device allocation failed")
+                                          : cuda_fail(e, "uploading the pair's fragments");
+  }
+  p->part_bytes = part;
+  *out = p;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_mlp_destroy(svdq_mlp_t p) {
+  if (!p) return SVDQ_OK;
+  DeviceGuard guard(p->device);
+  cudaDeviceSynchronize();
+  free_mlp(p);
+  delete p;
+  return SVDQ_OK;
+}
+
+svdq_status_t svdq_mlp_up_quantize(svdq_mlp_t p, const void* X, int64_t M, void* x_codes, void* x_scales, void* T,
+                                   void* stream) {
+  if (!p || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null pair or negative M");
+  if (M == 0) return SVDQ_OK;
+  if (!X || !x_codes || !x_scales || (p->rd > 0 && !T)) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!aligned16(X) || !aligned16(x_codes) || !aligned16(x_scales) || (T && !aligned16(T)))
+    return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  svdq_status_t st = mlp_check(p, M);
+  if (st != SVDQ_OK) return st;
+  const int64_t K = p->up->host.K, N = p->up->host.N;
+  const size_t xb = size_t(M) * K * 2, cb = size_t(M) * N / 2, sb = size_t(svdq_scales_bytes(M, N)),
+               tb = size_t(M) * p->down->r_pad * 2;
+  if (overlaps(X, xb, x_codes, cb) || overlaps(X, xb, x_scales, sb) || overlaps(x_codes, cb, x_scales, sb) ||
+      (T && (overlaps(T, tb, X, xb) || overlaps(T, tb, x_codes, cb) || overlaps(T, tb, x_scales, sb))))
+    return fail(SVDQ_ERR_INVALID_ARG, "X and the outputs must not overlap");
+  DeviceGuard guard(p->device);
+  return mlp_up(p, X, M, x_codes, x_scales, T, static_cast<cudaStream_t>(stream));
+}
+
+svdq_status_t svdq_mlp_forward(svdq_mlp_t p, const void* X, void* Y, int64_t M, void* stream) {
+  if (!p || M < 0) return fail(SVDQ_ERR_INVALID_ARG, "null pair or negative M");
+  if (M == 0) return SVDQ_OK;
+  if (!X || !Y) return fail(SVDQ_ERR_INVALID_ARG, "null buffer");
+  if (!aligned16(X) || !aligned16(Y)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  svdq_status_t st = mlp_check(p, M);
+  if (st != SVDQ_OK) return st;
+  svdq_layer* dn = p->down;
+  if (!dn->ws || dn->ws_M < M) return fail(SVDQ_ERR_WORKSPACE, "no down-layer workspace for this M (svdq_reserve)");
+  const size_t xb = size_t(M) * p->up->host.K * 2, yb = size_t(M) * dn->host.N * 2;
+  if (overlaps(X, xb, Y, yb)) return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap");
+  const WsLayout wu = ws_layout(p->up, p->up->ws_M, p->up->ws_staging);
+  const WsLayout wd = ws_layout(dn, dn->ws_M, dn->ws_staging);
+  if (overlaps(X, xb, p->up->ws, wu.Xs[0]) || overlaps(Y, yb, p->up->ws, wu.Xs[0]) ||
+      overlaps(X, xb, dn->ws, wd.Xs[0]) || overlaps(Y, yb, dn->ws, wd.Xs[0]))
+    return fail(SVDQ_ERR_INVALID_ARG, "X and Y must not overlap the layers' workspaces");
+  DeviceGuard guard(p->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* codes = dn->ws + wd.codes;
+  void* scales = dn->ws + wd.scales;
+  void* T = p->rd ? dn->ws + wd.T : nullptr;
+  st = mlp_up(p, X, M, codes, scales, T, s);
+  if (st != SVDQ_OK) return st;
+  return launch_k2(dn, codes, scales, T, Y, M, s);
+}
+
+svdq_status_t svdq_mlp_check_error(svdq_mlp_t p) {
+  if (!p) return fail(SVDQ_ERR_INVALID_ARG, "null pair");
+  const svdq_status_t a = svdq_check_error(p->up);
+  const svdq_status_t b = svdq_check_error(p->down);
+  return a != SVDQ_OK ? a : b;
+}
+
+svdq_status_t svdq_gelu_bf16(const void* Y, void* G, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!Y || !G))) return fail(SVDQ_ERR_INVALID_ARG, "null buffer or negative n");
+  if (n % 8) return fail(SVDQ_ERR_INVALID_ARG, "n must be a multiple of 8");
+  if (n == 0) return SVDQ_OK;
+  if (!aligned16(Y) || !aligned16(G)) return fail(SVDQ_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (Y != G && overlaps(Y, size_t(n) * 2, G, size_t(n) * 2))
+    return fail(SVDQ_ERR_INVALID_ARG, "Y and G must be the same buffer or not overlap");
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int e = gelu_launch(static_cast<const uint16_t*>(Y), static_cast<uint16_t*>(G), n, sms, stream);
+  if (e != 0) return cuda_fail(cudaError_t(e), "GELU kernel launch");
+  return SVDQ_OK;
+}
+
+}  // extern "C"
 
 // ------------------------------------------------------------------ AWQ-style W4A16 layer
 struct svdq_awq_layer {

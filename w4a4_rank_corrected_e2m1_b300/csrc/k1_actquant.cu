@@ -44,6 +44,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "nvfp4_block.cuh"
 #include "ptx.cuh"
 #include "svdq_internal.h"
 
@@ -92,46 +93,6 @@ __device__ __forceinline__ void li_loads(unsigned char* st, const unsigned char*
   constexpr int X_BYTES = 128 * 128, L_BYTES = R * 128;
   if (R > 0) ptx::bulk_load(st + X_BYTES, g + i * L_BYTES, L_BYTES, bar);
   ptx::bulk_load(st + X_BYTES + L_BYTES, g + kLIGroup * L_BYTES + i * 256, 256, bar);
-}
-
-// One 16-element NVFP4 block of a row: w holds its 16 bf16 values (8 words, low half first),
-// il their 1/lambda.  x^ = fl32(x * inv_lambda); scale code s8 = E4M3(fl32(amax / fl32(6 s_gX)))
-// from one product with the reciprocal, settled by the thresholds; codes = E2M1(fl32(x^ * rcp)).
-// Returns s8 and the 16 codes as two words (element 2j in the low nibble of byte j).
-__device__ __forceinline__ uint32_t quant_block(const uint32_t* w, const float* il, float inv_six, const float* s_thr,
-                                                const float* s_rcp, uint32_t* code0, uint32_t* code1) {
-  // straight-line code with short dependency chains (a pairwise max tree, no branch): the
-  // quantiser warps are few, so their throughput is set by latency, not by issue slots
-  float2 xh[8];
-  float a8[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float2 xv = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-    xh[k] = ptx::mul2_rn(xv, make_float2(il[2 * k], il[2 * k + 1]));
-    a8[k] = fmaxf(fabsf(xh[k].x), fabsf(xh[k].y));
-  }
-  const float m = fmaxf(fmaxf(fmaxf(fmaxf(a8[0], a8[1]), fmaxf(a8[2], a8[3])),
-                              fmaxf(fmaxf(a8[4], a8[5]), fmaxf(a8[6], a8[7]))),
-                        0.f);
-  int code = int(ptx::cvt_e4m3x2(0.f, __fmul_rn(m, inv_six)) & 0xFF);
-  code = code - (m < s_thr[code] ? 1 : 0) + (m >= s_thr[code + 1] ? 1 : 0);
-  const float rcp = s_rcp[code];
-  const float2 r2 = make_float2(rcp, rcp);
-  float2 q[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) q[k] = ptx::mul2_rn(xh[k], r2);
-  const uint32_t c0 = ptx::cvt_e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y);
-  const uint32_t c1 = ptx::cvt_e2m1x8(q[4].x, q[4].y, q[5].x, q[5].y, q[6].x, q[6].y, q[7].x, q[7].y);
-  // a zero scale gives zero codes (x * 0 may be -0, whose E2M1 code is not 0)
-  *code0 = code != 0 ? c0 : 0u;
-  *code1 = code != 0 ? c1 : 0u;
-  return uint32_t(code);
-}
-
-// Byte offset of the 32-bit word holding row `row`'s four scales of 64-column chunk c in the
-// tiled activation-scale layout.
-__device__ __forceinline__ int64_t scale_word_offset(int64_t row, int64_t c, int64_t KG) {
-  return ((row >> 7) * KG + c) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
 }
 
 __device__ bool k1_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, uint64_t limit_ns) {

@@ -117,6 +117,18 @@ struct K2Maps {
   alignas(64) unsigned char L2[128];   // CUtensorMap: L2^T         (bf16, r_pad x N, box 64 x 128, swizzle 128)
   alignas(64) unsigned char Y[128];    // CUtensorMap: Y            (bf16, N x M, box 64 x 32, swizzle 128)
 };
+// Fused MLP epilogue: the layer's output y feeds the next layer of an MLP pair through GELU, so
+// kernel 2 writes that layer's kernel-1 outputs for G = bf16(GELU(y)) instead of Y.
+struct K2Fuse {
+  const float* inv_lambda;    // N: the next layer's 1/lambda
+  const float* qtab;          // the next layer's quantiser tables (as K1Args::qtab)
+  float inv_six;              // the next layer's fl32(1 / (6 s_gX))
+  uint8_t* x_codes;           // M x N/2: the next layer's activation codes
+  uint8_t* x_scales;          // tiled, scale_groups(N) groups: its activation scales
+  const void* l1f;            // its L1' = diag(1/lambda) L1 in warp-MMA B-fragment order (k2_l1_fragments)
+  float* part;                // [2 S][M][rd]: partial G L1' of each unit and column half
+  int rd;                     // its kernel rank (0 or a multiple of 16, <= 64)
+};
 struct K2Args {
   const uint16_t* bias;       // N bf16
   int* err;                   // device error word
@@ -125,11 +137,29 @@ struct K2Args {
   float alpha;
   uint64_t wait_ns;           // limit of every bounded wait (nanoseconds)
   int stall;                  // failure-detection tests: the MMA thread waits on a barrier nothing completes
+  int unit_len = 1;           // tiles are taken in units of unit_len consecutive column tiles of one row block
+  K2Fuse fuse{};              // fused MLP epilogue (k2_fused_launch only)
 };
 // Default limit of the kernels' bounded waits: two seconds.
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 int k2_launch(const K2Maps& maps, const K2Args& a, int sm_count, void* stream);
 size_t k2_smem_bytes();
+// Fused MLP epilogue (kernel 2 of the up layer of a pair): maps.Y unused, a.fuse filled,
+// a.unit_len from k2_fused_unit_len; then k2_t_reduce_launch sums the partials into T.
+constexpr int kFuseMaxRank = 64;
+int k2_fused_unit_len(int64_t M, int64_t N, int pairs);
+int k2_fused_pairs(int sm_count);   // CTA pairs the fused kernel runs with on this device
+int64_t k2_fused_partials(int64_t M, int64_t N, int unit_len);   // partial sums per row (2 S)
+int k2_fused_launch(const K2Maps& maps, const K2Args& a, int sm_count, void* stream);
+// T[m][j] = bf16(fl32(sum over p of part[p][m][j]) * inv_alpha) for j < rd, 0 for rd <= j < r_pad
+int k2_t_reduce_launch(const float* part, int64_t P, int64_t M, int rd, int r_pad, float inv_alpha, uint16_t* T,
+                       void* stream);
+// Next-layer L1' (K x rd bf16 bits, row-major) -> warp-MMA B fragments: for 16-row step s and
+// pair np of 8-column groups, lane l's 16 bytes are {b0, b1} of group 2 np then of 2 np + 1,
+// b0 = rows 16 s + 2 (l % 4) + {0, 1} and b1 = rows + 8, column 16 np + 8 g + l / 4.
+void k2_l1_fragments(const uint16_t* L1p, int64_t K, int rd, uint16_t* out);
+// Elementwise bf16(GELU(y)) with the fused epilogue's arithmetic.
+int gelu_launch(const uint16_t* Y, uint16_t* G, int64_t n, int sm_count, void* stream);
 
 // ------------------------------------------------------------------ INT4 variant (int4_path.cu)
 // Symmetric INT4 groups: nibble q + 8, q in [-7, 7], one float32 scale per 64 elements along K.

@@ -107,6 +107,12 @@ _SIGS = {
     "svdq_int4_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "svdq_int4_check_error": (_i32, [_vp]),
     "svdq_int4_destroy": (_i32, [_vp]),
+    "svdq_mlp_create": (_i32, [_vp, _vp, _i64, ctypes.POINTER(_vp)]),
+    "svdq_mlp_destroy": (_i32, [_vp]),
+    "svdq_mlp_up_quantize": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "svdq_mlp_forward": (_i32, [_vp, _vp, _vp, _i64, _vp]),
+    "svdq_mlp_check_error": (_i32, [_vp]),
+    "svdq_gelu_bf16": (_i32, [_vp, _vp, _i64, _vp]),
     "svdq_status_string": (ctypes.c_char_p, [_i32]),
     "svdq_last_error": (ctypes.c_char_p, []),
 }
@@ -386,6 +392,44 @@ class Int4Layer:
 
     def check_error(self):
         check(LIB.svdq_int4_check_error(self.h), "svdq_int4_check_error")
+
+
+# ------------------------------------------------------------------ MLP pair
+class Mlp:
+    """Two packed layers with GELU between them, run with the fused epilogue (wraps an
+    svdq_mlp_t).  The layers must outlive the pair and have workspaces for the M they run."""
+
+    def __init__(self, up: Layer, down: Layer, M_max: int):
+        h = _vp()
+        check(LIB.svdq_mlp_create(up.h, down.h, M_max, ctypes.byref(h)), "svdq_mlp_create")
+        self.h = h
+        self.up, self.down, self.M_max = up, down, M_max
+
+    def close(self):
+        if getattr(self, "h", None):
+            LIB.svdq_mlp_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def up_quantize(self, X, M, x_codes, x_scales, T=None, stream=None):
+        check(LIB.svdq_mlp_up_quantize(self.h, _ptr(X), M, _ptr(x_codes), _ptr(x_scales), _ptr(T), _stream(stream)),
+              "svdq_mlp_up_quantize")
+
+    def forward(self, X, Y, M, stream=None):
+        check(LIB.svdq_mlp_forward(self.h, _ptr(X), _ptr(Y), M, _stream(stream)), "svdq_mlp_forward")
+
+    def check_error(self):
+        check(LIB.svdq_mlp_check_error(self.h), "svdq_mlp_check_error")
+
+
+def gelu_bf16(Y, G, n, stream=None):
+    """G = bf16(GELU(Y)) elementwise on n bf16 values (the fused epilogue's arithmetic)."""
+    check(LIB.svdq_gelu_bf16(_ptr(Y), _ptr(G), n, _stream(stream)), "svdq_gelu_bf16")
 
 
 # ------------------------------------------------------------------ AWQ-style W4A16 layer

@@ -146,6 +146,57 @@ def make_x(w: Workload, M: int, seed: int) -> np.ndarray:
     return make(scaled(w, M=M), seed=seed)["X"]
 
 
+def make_weights(w: Workload, seed: int | None = None) -> Dict[str, np.ndarray]:
+    """W (N x K) and bias (N) of the recipe alone, from their own generator (the second layer of
+    an MLP pair, whose input is the first layer's activated output, not drawn).  Draw order: W,
+    spike factors U, V, bias."""
+    rng = np.random.default_rng((w.seed if seed is None else seed, 1))
+    N, K = w.N, w.K
+    W = rng.standard_normal((N, K)) * (1.0 / np.sqrt(K))
+    if w.spike_rank:
+        U, _ = np.linalg.qr(rng.standard_normal((N, w.spike_rank)))
+        V, _ = np.linalg.qr(rng.standard_normal((K, w.spike_rank)))
+        W += w.spike_sigma * (U @ V.T)
+    b = rng.standard_normal(N) * w.bias_std
+    return {"W": f64_to_bf16_bits(W), "bias": f64_to_bf16_bits(b)}
+
+
+@dataclasses.dataclass(frozen=True)
+class PairWorkload:
+    """An MLP pair: up (M x K -> N_up), GELU, down (N_up -> N).  X, W_up and b_up come from
+    make(up); W_down and b_down from make_weights(down)."""
+    name: str
+    up: Workload
+    down: Workload
+
+    def __post_init__(self):
+        assert self.down.K == self.up.N and self.down.M == self.up.M
+
+
+# the FLUX transformer block's feed-forward (3072 -> 12288 -> GELU -> 3072)
+MLP_PAIR = PairWorkload("flux_mlp_pair", MLP_UP, MLP_DOWN)
+
+
+def pair(name: str, M: int, K: int, N_up: int, N: int, r_up: int, r_down: int) -> PairWorkload:
+    """A smaller pair with the FLUX pair's value recipes."""
+    return PairWorkload(name, scaled(MLP_UP, name=name + "_up", M=M, K=K, N=N_up, rank=r_up,
+                                     n_outlier=max(1, int(round(0.01 * K)))),
+                        scaled(MLP_DOWN, name=name + "_down", M=M, K=N_up, N=N, rank=r_down))
+
+
+def pair_parity_cases() -> List[PairWorkload]:
+    """Small pairs: ragged M and N_up, every supported down rank, one column tile per unit
+    (small M) and longer units (M spanning several row blocks)."""
+    return [
+        pair("pair_tiny", 64, 256, 256, 128, 16, 16),
+        pair("pair_ragged", 300, 512, 320, 272, 32, 32),
+        pair("pair_r64", 257, 768, 1024, 512, 32, 64),
+        pair("pair_r48_small_m", 40, 256, 2048, 256, 16, 48),
+        pair("pair_down_r0", 130, 256, 512, 256, 16, 0),
+        pair("pair_units", 2560, 256, 4096, 256, 32, 32),
+    ]
+
+
 def parity_cases() -> List[Workload]:
     """Small cases: several tiles of every kernel plus a ragged tail in M."""
     return [
