@@ -43,13 +43,13 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on 
 # captures summarised under profiles/, keyed by the workload and by a hash of the kernel's
 # sources at capture time: a kernel edited since then reports null traffic.
 NCU_TRAFFIC = {
-    ("flux_mlp_up", "k1_actquant"): ("ec467875c6f22f34", 28.56e6 + 256.0),
-    ("flux_mlp_up", "k2_fp4gemm"): ("fbb14fff96e80e4f", 33.06e6 + 63.16e6),
-    ("flux_mod", "awq_gemv"): ("666902da617b3e67", 35.47e6 + 0.0),
+    ("flux_mlp_up", "k1_actquant"): ("e743785140e04503", 28561152.0 + 0.0),
+    ("flux_mlp_up", "k2_fp4gemm"): ("14e3f5c452d87d7c", 32932608.0 + 63176960.0),
+    ("flux_mod", "awq_gemv"): ("c28e9c1a0fcd68d8", 35471616.0 + 0.0),
 }
 KERNEL_SOURCES = {
-    "k1_actquant": ["k1_actquant.cu", "ptx.cuh", "svdq_internal.h"],
-    "k2_fp4gemm": ["k2_fp4gemm.cu", "ptx.cuh", "svdq_internal.h"],
+    "k1_actquant": ["k1_actquant.cu", "nvfp4_block.cuh", "ptx.cuh", "svdq_internal.h"],
+    "k2_fp4gemm": ["k2_fp4gemm.cu", "nvfp4_block.cuh", "ptx.cuh", "svdq_internal.h"],
     "awq_gemv": ["awq_gemv.cu", "ptx.cuh", "svdq_internal.h"],
 }
 
@@ -82,7 +82,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="flux_mlp_up", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--workload", default="flux_mlp_up",
+                    choices=sorted(synthetic.WORKLOADS) + [synthetic.MLP_PAIR.name])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="time the headline workload only")
@@ -301,10 +302,11 @@ class L2Flush:
     def __init__(self, torch):
         self.torch = torch
         self.buf = torch.ones(64 << 20, dtype=torch.int32, device="cuda")
-        self.acc = torch.empty((), dtype=torch.int64, device="cuda")
+        self.acc = torch.empty((), dtype=torch.int32, device="cuda")
 
     def __call__(self):
-        self.torch.sum(self.buf, dim=0, out=self.acc)
+        # int32 in and out: one reduction kernel, no widening copy of the buffer first
+        self.torch.sum(self.buf, dim=0, dtype=self.torch.int32, out=self.acc)
 
 
 def k1_bytes(M, K, rank):
@@ -777,8 +779,72 @@ def run_reference_awq(args, w):
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
 
 
+# ------------------------------------------------------------------ MLP pair (fused epilogue)
+PAIR_METRIC = "FLUX MLP pair (3072 -> 12288 -> GELU -> 3072) forward with the fused epilogue: TFLOP/s"
+
+
+def pair_flops(pw):
+    up, dn = pw.up, pw.down
+    return 2.0 * up.M * (up.N * up.K + dn.N * dn.K) + 2.0 * up.M * (up.rank * (up.K + up.N) + dn.rank * (dn.K + dn.N))
+
+
+def run_pair(args, pw):
+    """The MLP pair, fused and unfused (its own JSON line; one GPU)."""
+    import torch
+    from w4a4_rank_corrected_e2m1_b300 import svdq
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    stream = torch.cuda.current_stream()
+    clocks = Clocks(torch.cuda.current_device())
+    out = measure_mlp_pair(torch, svdq, pw, stream, L2Flush(torch), reps=args.steps, warm=args.warmup)
+    clk = clocks.stop()
+    us = out["cold_l2"]["fused_us"]
+    print(json.dumps({
+        "metric": PAIR_METRIC, "value": pair_flops(pw) / (us * 1e-6) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us * 1e-3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4(e2m1,e4m3)+bf16, f32 accumulate", "data": "synthetic",
+        "config": {"workload": pw.name, "M": pw.up.M, "K": pw.up.K, "N_up": pw.up.N, "N": pw.down.N,
+                   "ranks": [pw.up.rank, pw.down.rank],
+                   "l2": "flushed before every timed step (a 256 MiB read, outside the timed events)"},
+        "tokens_per_s": pw.up.M / (us * 1e-6), "pair": out,
+        "gpu_launches": 4 * args.steps, "clocks": clk}), flush=True)
+
+
+def run_reference_pair(args, pw):
+    """The oracle's MLP pair on the host cores, on a bounded sample of token rows."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from oracle import svdquant as sq
+    d = synthetic.make(pw.up)
+    rows = 16
+    up = sq.pack(d["W"], d["bias"], pw.up.rank, Xcal_bits=d["X"][:256])
+    G = sq.f64_to_bf16(sq.gelu(sq.bf16_to_f64(sq.f64_to_bf16(sq.forward(d["X"][:256], up)))))
+    wd = synthetic.make_weights(pw.down)
+    down = sq.pack(wd["W"], wd["bias"], pw.down.rank, Xcal_bits=G)
+    steps = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for i in range(steps):
+        sq.mlp_pair_forward(d["X"][rows * i: rows * (i + 1)], up, down)
+    dt = (time.perf_counter() - t0) / steps
+    val = pair_flops(pw) * rows / pw.up.M / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": PAIR_METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": 0, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": pw.name, "M": pw.up.M, "K": pw.up.K, "N_up": pw.up.N, "N": pw.down.N},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+                         "threads": blas_threads(), "kind": "oracle",
+                         "sample": f"oracle pair forward on {rows} token rows per step, {steps} steps"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload == synthetic.MLP_PAIR.name:
+        (run_reference_pair if args.impl == "reference" else run_pair)(args, synthetic.MLP_PAIR)
+        return
     w = synthetic.get(args.workload)
     if args.impl == "reference":
         if w in synthetic.AWQ_WORKLOADS:

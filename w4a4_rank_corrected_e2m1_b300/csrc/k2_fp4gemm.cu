@@ -169,18 +169,19 @@ __device__ __forceinline__ void store64(const void* map, unsigned char* stg, con
   }
 }
 
-// alpha * acc + bias -> 16 packed bf16 pairs for 32 columns (the arithmetic of convert64)
+// alpha * acc + bias -> 16 packed bf16 pairs for 32 columns (convert64's arithmetic, two fused
+// multiply-adds per packed instruction)
 __device__ __forceinline__ void convert32(const uint32_t* r, const uint16_t* bias, float alpha, uint32_t* out) {
+  const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const uint4 bb = *reinterpret_cast<const uint4*>(bias + 8 * v);
     const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const float b0 = __uint_as_float(bw[u] << 16), b1 = __uint_as_float(bw[u] & 0xFFFF0000u);
-      const float y0 = fmaf(alpha, __uint_as_float(r[8 * v + 2 * u]), b0);
-      const float y1 = fmaf(alpha, __uint_as_float(r[8 * v + 2 * u + 1]), b1);
-      out[4 * v + u] = ptx::pack_bf16x2(y0, y1);
+      const float2 b = make_float2(__uint_as_float(bw[u] << 16), __uint_as_float(bw[u] & 0xFFFF0000u));
+      const float2 y = ptx::fma2_rn(a2, make_float2(__uint_as_float(r[8 * v + 2 * u]), __uint_as_float(r[8 * v + 2 * u + 1])), b);
+      out[4 * v + u] = ptx::pack_bf16x2(y.x, y.y);
     }
   }
 }

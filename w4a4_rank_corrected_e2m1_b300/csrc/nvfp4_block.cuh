@@ -78,9 +78,32 @@ __device__ __forceinline__ float gelu_f32(float y) {
   return y <= 0.0f ? y * q : y * (1.0f - q);
 }
 
-// bf16 pair (low half first) -> bf16(GELU) pair
+// bf16 pair (low half first) -> bf16(GELU) pair: gelu_f32 on both halves with packed float32
+// operations (two IEEE operations per instruction), bit for bit the same values.  The exponent
+// is formed negated, z^2 - P(t) from the negated polynomial, and scaled by -log2 e: negation
+// commutes with rounding to nearest even, so every rounded value is gelu_f32's up to sign.
 __device__ __forceinline__ uint32_t gelu_bf16x2(uint32_t w) {
-  return ptx::pack_bf16x2(gelu_f32(__uint_as_float(w << 16)), gelu_f32(__uint_as_float(w & 0xFFFF0000u)));
+  const float2 y = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  const float2 nz = ptx::mul2_rn(make_float2(fabsf(y.x), fabsf(y.y)),
+                                 make_float2(-0.70710678118654752f, -0.70710678118654752f));   // -z
+  const float2 d = ptx::fma2_rn(make_float2(-0.5f, -0.5f), nz, make_float2(1.0f, 1.0f));     // 1 + z/2
+  const float2 t = make_float2(ptx::rcp_approx(d.x), ptx::rcp_approx(d.y));
+  auto c2 = [](float c) { return make_float2(c, c); };
+  float2 pn = ptx::fma2_rn(c2(-0.17087277f), t, c2(0.82215223f));                             // -P(t)
+  pn = ptx::fma2_rn(pn, t, c2(-1.48851587f));
+  pn = ptx::fma2_rn(pn, t, c2(1.13520398f));
+  pn = ptx::fma2_rn(pn, t, c2(-0.27886807f));
+  pn = ptx::fma2_rn(pn, t, c2(0.18628806f));
+  pn = ptx::fma2_rn(pn, t, c2(-0.09678418f));
+  pn = ptx::fma2_rn(pn, t, c2(-0.37409196f));
+  pn = ptx::fma2_rn(pn, t, c2(-1.00002368f));
+  pn = ptx::fma2_rn(pn, t, c2(1.26551223f));
+  const float2 u = ptx::mul2_rn(ptx::fma2_rn(nz, nz, pn), c2(-1.44269504088896341f));        // (-z^2 + P) log2 e
+  const float2 e = make_float2(ptx::ex2_approx(u.x), ptx::ex2_approx(u.y));
+  const float2 q = ptx::mul2_rn(ptx::mul2_rn(c2(0.5f), t), e);                                 // Q(|y|)
+  const float2 om = ptx::fma2_rn(q, c2(-1.0f), c2(1.0f));                                     // 1 - Q
+  const float2 g = ptx::mul2_rn(y, make_float2(y.x <= 0.0f ? q.x : om.x, y.y <= 0.0f ? q.y : om.y));
+  return ptx::pack_bf16x2(g.x, g.y);
 }
 
 }  // namespace svdq
