@@ -465,8 +465,14 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
   const int64_t M = a.M, K = a.K;
   const int64_t KG = scale_groups(K);
   const int nchunks = int(K / 64);
-  const int nsteps = (nchunks + C::CH - 1) / C::CH;
-  const int64_t row0 = int64_t(blockIdx.x) * kTallRows;
+  const int nsteps_all = (nchunks + C::CH - 1) / C::CH;
+  // this CTA's 32-row tile and its stages [s_begin, s_begin + nsteps) of K (a.tsplit CTAs per
+  // tile at small M, one otherwise)
+  const int tsplit = a.tsplit, sp = int(blockIdx.x) % tsplit, rtile = int(blockIdx.x) / tsplit;
+  const int s_begin = tsplit > 1 ? sp * a.tsteps : 0;
+  const int s_end = tsplit > 1 ? min(nsteps_all, s_begin + a.tsteps) : nsteps_all;
+  const int nsteps = s_end > s_begin ? s_end - s_begin : 0;
+  const int64_t row0 = int64_t(rtile) * kTallRows;
 
   for (int i = threadIdx.x; i < 256; i += blockDim.x) (i < 128 ? s_thr[i] : s_rcp[i - 128]) = a.qtab[i];
   if (threadIdx.x == 0) {
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       for (int st_i = 0; st_i < pre; ++st_i) {
         unsigned char* st = ring + st_i * C::STAGE_BYTES;
         ptx::mbar_arrive_expect_tx(&full[st_i], C::X_BYTES + C::LI_BYTES);
-        tall_li_loads<R>(st + C::X_BYTES, a.LI, st_i, &full[st_i]);
+        tall_li_loads<R>(st + C::X_BYTES, a.LI, s_begin + st_i, &full[st_i]);
       }
       ptx::griddep_wait();
       int stage = 0, issued = 0;
@@ -509,12 +515,12 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
           if (!k1_wait(&empty[stage], phase ^ 1u, &abort_flag, a.err, a.wait_ns)) break;
           ptx::fence_proxy_async_smem();   // ordinary-load reads of the stage before the refill
           ptx::mbar_arrive_expect_tx(&full[stage], C::X_BYTES + C::LI_BYTES);
-          tall_li_loads<R>(st + C::X_BYTES, a.LI, j, &full[stage]);
+          tall_li_loads<R>(st + C::X_BYTES, a.LI, s_begin + j, &full[stage]);
         }
         // a chunk index past K reads as zeros (out-of-range box) and still delivers its bytes
 #pragma unroll
         for (int cc = 0; cc < C::CH; ++cc)
-          ptx::tma_load_2d(st + cc * C::X_TILE, &xmap, &full[stage], 64 * (C::CH * j + cc), int(row0));
+          ptx::tma_load_2d(st + cc * C::X_TILE, &xmap, &full[stage], 64 * (C::CH * (s_begin + j) + cc), int(row0));
         if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
       }
       for (int i = 0; i < C::STAGES; ++i) {       // every copy issued has landed
@@ -569,8 +575,8 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
     const int r = (warp % C::WPC) * 8 + g;                      // r % 8 == g: the swizzle row
     const int64_t row = row0 + r;
     const bool live = row < M;
-    unsigned char* code_p = a.x_codes + row * (K / 2) + cc * 32 + 8 * t;
-    unsigned char* scale_p = a.x_scales + scale_word_offset(row, cc, KG);
+    unsigned char* code_p = a.x_codes + row * (K / 2) + (C::CH * s_begin + cc) * 32 + 8 * t;
+    unsigned char* scale_p = a.x_scales + scale_word_offset(row, C::CH * s_begin + cc, KG);
     const int xoff = cc * C::X_TILE + r * 128;
     const int u0off = xoff + (((2 * t) ^ g) << 4), u1off = xoff + (((2 * t + 1) ^ g) << 4);
     const int iloff = C::X_BYTES + C::CH * C::L_BYTES + cc * 256 + 64 * t;
@@ -598,7 +604,7 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       if (lane == 0) ptx::mbar_arrive(&empty[stage]);
       if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
 
-      if (C::CH * j + cc >= nchunks) continue;
+      if (C::CH * (s_begin + j) + cc >= nchunks) continue;
       uint32_t code0, code1;
       const uint32_t s8 = quant_block(w, il, a.inv_six, s_thr, s_rcp, &code0, &code1);
       // the quad's four scale bytes of this row form one 32-bit word of the tiled layout
@@ -608,8 +614,9 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       if (live) *reinterpret_cast<uint2*>(code_p) = make_uint2(code0, code1);
       if (t == 0) *reinterpret_cast<uint32_t*>(scale_p) = word;
     }
-    // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM
-    for (int c = nchunks; c < KG; ++c)
+    // scale groups past K (K not a multiple of 256) read as zero scales by the GEMM (written by
+    // the CTA holding the last stage)
+    for (int c = nchunks; c < KG && s_end == nsteps_all; ++c)
       if (c % C::CH == cc && t == 0) *reinterpret_cast<uint32_t*>(a.x_scales + scale_word_offset(row, c, KG)) = 0u;
     // rows after the last 32-row tile, up to the end of its 128-row scale tile, belong to no
     // CTA: the last one writes their scales as zeros
@@ -625,6 +632,11 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
   if constexpr (R > 0) {
     const int64_t row = row0 + lane;
     uint4* trow = reinterpret_cast<uint4*>(a.T + row * a.r_pad);
+    // with a K split, the tile's CTAs form a cluster: each keeps its float32 share [R][32 rows]
+    // in shared memory (after the ring's reduction buffer) and cluster rank 0 adds the shares in
+    // split order through distributed shared memory
+    const bool split = tsplit > 1;
+    float* part = reinterpret_cast<float*>(ring) + 3 * 32 * R;
     // 32 columns of T from TMEM (plus the other warps' blocks in `red`), scaled, to bf16
     auto emit = [&](int cb, const uint32_t* v, const float* red, bool ok) {
 #pragma unroll
@@ -640,10 +652,11 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
               y[e] = __uint_as_float(v[j + 2 * u + e]);
               if (red)
                 y[e] = ((y[e] + red[col * 32 + lane]) + red[(R + col) * 32 + lane]) + red[(2 * R + col) * 32 + lane];
+              if (split) part[col * 32 + lane] = ok ? y[e] : 0.f;   // this split's share, float32
             }
             o[u] = ok ? ptx::pack_bf16x2(y[0] * a.inv_alpha, y[1] * a.inv_alpha) : 0u;
           }
-          if (row < M) trow[(cb + j) / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+          if (!split && row < M) trow[(cb + j) / 8] = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
     };
@@ -656,7 +669,7 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       if (warp < 4) {
         // the MMAs have completed before TMEM is read (or freed), also after an abort
         k1_drain(&done, 0, a.err);
-        const bool ok = !abort_flag;
+        const bool ok = !abort_flag && nsteps > 0;   // (an empty split contributes zeros)
         ptx::tc_fence_after();
         if (warp > 0) {
 #pragma unroll
@@ -680,11 +693,15 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
           }
         }
       }
-    } else if (warp == 0) {
+    } else {
+      // with a K split the share goes into the ring: every quantiser warp is past its last stage
+      if (split && warp < kQWarps) ptx::bar_sync(1, 32 * kQWarps);
+    }
+    if (!C::STACK && warp == 0) {
       // one product per chunk: T is TMEM lanes 0..31 (read once the MMAs have completed, also
       // after an abort)
       k1_drain(&done, 0, a.err);
-      const bool ok = !abort_flag;
+      const bool ok = !abort_flag && nsteps > 0;
       ptx::tc_fence_after();
 #pragma unroll
       for (int cb = 0; cb < R; cb += 32) {
@@ -694,13 +711,48 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
         emit(cb, v, nullptr, ok);
       }
     }
-    if (warp == 0 && row < M)
+    if (!split && warp == 0 && row < M)
       for (int j = R; j < a.r_pad; j += 8) trow[j / 8] = make_uint4(0, 0, 0, 0);
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kMma) {
       ptx::tc_fence_after();
       ptx::tmem_dealloc(tmem_slot, C::TMEM_COLS);
+    }
+    if (split) {
+      ptx::cluster_sync();                        // every share is in its CTA's shared memory
+      if (sp == 0) {
+        // T = (sum of the shares in split order) / alpha, 32 rows x r_pad columns (zeros past R);
+        // every share is loaded before any is added
+        const uint32_t own = ptx::smem_u32(part);
+        for (int e = threadIdx.x; e < 32 * (a.r_pad / 2); e += blockDim.x) {
+          const int rr = e % 32, cp = e / 32;
+          uint32_t o = 0u;
+          if (2 * cp < R) {
+            float p0[kK1TallMaxSplit], p1[kK1TallMaxSplit];
+            const uint32_t off0 = uint32_t(((2 * cp) * 32 + rr) * 4), off1 = off0 + 32 * 4;
+#pragma unroll
+            for (int q = 0; q < kK1TallMaxSplit; ++q) {
+              if (q < tsplit) {
+                const uint32_t base = ptx::mapa(own, uint32_t(q));
+                p0[q] = ptx::ld_cluster_f32(base + off0);
+                p1[q] = ptx::ld_cluster_f32(base + off1);
+              }
+            }
+            float s0 = p0[0], s1 = p1[0];
+#pragma unroll
+            for (int q = 1; q < kK1TallMaxSplit; ++q) {
+              if (q < tsplit) {
+                s0 += p0[q];
+                s1 += p1[q];
+              }
+            }
+            o = ptx::pack_bf16x2(s0 * a.inv_alpha, s1 * a.inv_alpha);
+          }
+          if (row0 + rr < M) reinterpret_cast<uint32_t*>(a.T + (row0 + rr) * a.r_pad)[cp] = o;
+        }
+      }
+      ptx::cluster_sync();                        // rank 0 has read every share: all may exit
     }
   }
 }
@@ -717,7 +769,7 @@ int launch_tall(const XMap& map, const K1Args& a, const K1Plan& p, cudaStream_t 
     attr_done[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.row_tiles, 1, 1);
+  cfg.gridDim = dim3(unsigned(p.row_tiles * p.nsplit), 1, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
@@ -726,7 +778,19 @@ int launch_tall(const XMap& map, const K1Args& a, const K1Plan& p, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return int(cudaLaunchKernelEx(&cfg, k1_tall_kernel<R>, map, a));
+  cudaLaunchAttribute attr2[2] = {attr[0], {}};
+  if (p.nsplit > 1) {                             // a tile's split CTAs form one cluster
+    attr2[1].id = cudaLaunchAttributeClusterDimension;
+    attr2[1].val.clusterDim.x = unsigned(p.nsplit);
+    attr2[1].val.clusterDim.y = 1;
+    attr2[1].val.clusterDim.z = 1;
+    cfg.attrs = attr2;
+    cfg.numAttrs = 2;
+  }
+  K1Args b = a;
+  b.tsplit = p.nsplit;
+  b.tsteps = p.chunks_per_split / C::CH;
+  return int(cudaLaunchKernelEx(&cfg, k1_tall_kernel<R>, map, b));
 }
 
 template <int R>
@@ -758,7 +822,6 @@ int launch_t(const XMap& map, const K1Args& a, const K1Plan& p, cudaStream_t s) 
 }  // namespace
 
 K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count) {
-  (void)rank;
   K1Plan p;
   const int nchunks = int(K / 64);
   // enough 32-row tiles to give every other SM one: whole-K CTAs, no split
@@ -767,8 +830,21 @@ K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count) {
   if (ceil_div(M, kTallRows) * 2 >= sm_count || nchunks <= 96) {
     p.tall = true;
     p.row_tiles = int(ceil_div(M, kTallRows));
-    p.nsplit = 1;
-    p.chunks_per_split = nchunks;
+    // with fewer tiles than half the SMs, every CTA would stream the whole of K for its 32 rows
+    // (the kernel's time would not fall with M): split K over up to kK1TallMaxSplit CTAs a tile
+    // (one thread-block cluster), in whole stages, so that the tiles' CTAs fill the SMs once
+    const int ch = rank <= 96 ? 4 : 2;
+    const int nsteps = int(ceil_div(nchunks, ch));
+    int ns = 1;
+    if (p.row_tiles * 2 < sm_count && p.row_tiles > 0) {
+      ns = sm_count / p.row_tiles;
+      ns = ns > kK1TallMaxSplit ? kK1TallMaxSplit : ns;
+      ns = ns > nsteps ? nsteps : ns;
+      ns = ns < 1 ? 1 : ns;
+    }
+    const int steps = int(ceil_div(nsteps, ns));
+    p.nsplit = int(ceil_div(nsteps, steps));       // no empty split
+    p.chunks_per_split = steps * ch;
     return p;
   }
   p.row_tiles = int(ceil_div(M, kRows));

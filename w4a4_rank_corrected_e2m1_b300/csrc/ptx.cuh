@@ -289,6 +289,13 @@ __device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t caddr) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// 32-bit load of a shared-memory word of a CTA of this cluster (address from mapa).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+  return v;
+}
+
 // 32-bit store to a shared-memory word of a CTA of this cluster (address from mapa).
 __device__ __forceinline__ void st_cluster_u32(uint32_t caddr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");

@@ -94,6 +94,8 @@ struct K1Args {
   int* err;                   // device error word (bounded waits)
   uint64_t wait_ns;           // limit of every bounded wait (nanoseconds)
   int stall;                  // failure-detection tests: the MMA warp waits on a barrier nothing completes
+  int tsplit = 1;             // whole-K path: CTAs per 32-row tile, each over tsteps stages of K
+  int tsteps = 0;
 };
 struct K1Plan {
   bool tall = false;          // 32-row tiles over the whole of K (no split) instead of 128-row split tiles
@@ -101,6 +103,7 @@ struct K1Plan {
 };
 K1Plan k1_plan(int64_t M, int64_t K, int rank, int sm_count);
 constexpr int kK1MaxSplit = 8;   // K splits per 128-row tile
+constexpr int kK1TallMaxSplit = 8;    // K splits per 32-row tile (one portable cluster; small M)
 // Workspace bytes of the split-K partial sums and the arrival words for M rows.
 size_t k1_partial_bytes(int64_t M, int rank);
 size_t k1_arrival_bytes(int64_t M);
