@@ -43,9 +43,9 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on 
 # captures summarised under profiles/, keyed by the workload and by a hash of the kernel's
 # sources at capture time: a kernel edited since then reports null traffic.
 NCU_TRAFFIC = {
-    ("flux_mlp_up", "k1_actquant"): ("e743785140e04503", 28561152.0 + 0.0),
-    ("flux_mlp_up", "k2_fp4gemm"): ("14e3f5c452d87d7c", 32932608.0 + 63176960.0),
-    ("flux_mod", "awq_gemv"): ("c28e9c1a0fcd68d8", 35471616.0 + 0.0),
+    ("flux_mlp_up", "k1_actquant"): ("a899016892787335", 28570880.0 + 0.0),
+    ("flux_mlp_up", "k2_fp4gemm"): ("f40d52cc438d70d5", 32619520.0 + 63159296.0),
+    ("flux_mod", "awq_gemv"): ("8e37fe927aa59519", 35471616.0 + 0.0),
 }
 KERNEL_SOURCES = {
     "k1_actquant": ["k1_actquant.cu", "nvfp4_block.cuh", "ptx.cuh", "svdq_internal.h"],
