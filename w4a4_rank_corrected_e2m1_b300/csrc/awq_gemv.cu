@@ -8,9 +8,9 @@
 // The work is one pass over the packed weights (HBM-bound: 0.5 byte per weight plus 8 bytes
 // per group of 64), streamed by one block per SM: a producer warp moves the block's
 // contiguous run of weight rows (codes, then the rows' (scale, zero point) pairs) through a
-// shared-memory ring with bulk copies, and sixteen warps consume it (one weight row each per
-// stage), keeping the ALU cost per
-// weight small:
+// shared-memory ring with bulk copies, and sixteen warps consume it (two weight rows each per
+// stage where three stages of that size fit: two independent chains per warp, one read of x'
+// for both), keeping the ALU cost per weight small:
 //   * the block's rows of x' sit in shared memory in fp16, 32-channel segments padded to 80
 //     bytes so that a warp's 16-byte reads are conflict-free;
 //   * a lane takes 16 bytes of codes (32 weights, half a group) at a time; LOP3s turn two codes
@@ -81,7 +81,9 @@ struct AwqPlan {
   size_t stage_bytes, xs_bytes, smem;
 };
 
-__host__ __device__ constexpr int64_t stage_rows_for(int64_t K) { return K <= 6144 ? 16 : (K <= 12288 ? 8 : 4); }
+__host__ __device__ constexpr int64_t stage_rows_for(int64_t K) {
+  return K <= 3072 ? 32 : (K <= 6144 ? 16 : (K <= 12288 ? 8 : 4));   // two rows a warp where three stages still fit
+}
 
 __device__ __forceinline__ unsigned char* xs_row(unsigned char* xs, int m, int64_t K) {
   return xs + size_t(m) * xs_bytes_per_row(K);
@@ -231,28 +233,40 @@ __global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, i
       if (!bounded_wait(&full[stage], phase, &abort_flag)) break;
       const unsigned char* st = ring + size_t(stage) * stage_bytes;
       const int64_t row0 = r_begin + int64_t(j) * rs;
-      for (int rr = warp; rr < rs; rr += kWarps) {
-        const int64_t n = row0 + rr;
-        if (n >= r_end) break;
-        const uint32_t crow = ptx::smem_u32(st + size_t(rr) * codes_row);
-        const uint32_t szrow = ptx::smem_u32(st + size_t(rs) * codes_row + size_t(rr) * sz_row);
-        float part[MB];
+      // two weight rows per warp at a time (rr and rr + kWarps): two independent chains, and each
+      // x' read from shared memory serves both
+      for (int rr = warp; rr < rs; rr += 2 * kWarps) {
+        const int64_t n0 = row0 + rr;
+        if (n0 >= r_end) break;
+        const bool two = rr + kWarps < rs && n0 + kWarps < r_end;
+        const int rb = two ? rr + kWarps : rr;     // the second row (the first again when absent)
+        uint32_t crow[2], szrow[2];
+        crow[0] = ptx::smem_u32(st + size_t(rr) * codes_row);
+        crow[1] = ptx::smem_u32(st + size_t(rb) * codes_row);
+        szrow[0] = ptx::smem_u32(st + size_t(rs) * codes_row + size_t(rr) * sz_row);
+        szrow[1] = ptx::smem_u32(st + size_t(rs) * codes_row + size_t(rb) * sz_row);
+        float part[2][MB];
 #pragma unroll
-        for (int m = 0; m < MB; ++m) part[m] = 0.f;
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int m = 0; m < MB; ++m) part[h][m] = 0.f;
         // three 32-weight chunks per lane at a time (K = 3072 in one pass), all loaded first
         constexpr int kU = 3;
         for (int sg0 = lane; sg0 < nseg; sg0 += 32 * kU) {
-          uint4 c[kU];
-          float2 sz[kU];
+          uint4 c[2][kU];
+          float2 sz[2][kU];
 #pragma unroll
           for (int i = 0; i < kU; ++i) {
             const int sgi = sg0 + 32 * i;
-            if (sgi < nseg) {
-              c[i] = ptx::lds_v4(crow + uint32_t(sgi) * 16u);
-              sz[i] = ptx::lds_f32x2(szrow + uint32_t(sgi >> 1) * 8u);    // scale, zero point
-            } else {
-              c[i] = make_uint4(0x64646464u, 0x64646464u, 0x64646464u, 0x64646464u);
-              sz[i] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (sgi < nseg) {
+                c[h][i] = ptx::lds_v4(crow[h] + uint32_t(sgi) * 16u);
+                sz[h][i] = ptx::lds_f32x2(szrow[h] + uint32_t(sgi >> 1) * 8u);    // scale, zero point
+              } else {
+                c[h][i] = make_uint4(0x64646464u, 0x64646464u, 0x64646464u, 0x64646464u);
+                sz[h][i] = make_float2(0.f, 0.f);
+              }
             }
           }
 #pragma unroll
@@ -261,52 +275,64 @@ __global__ void __launch_bounds__(kThreads + 32, 1) awq_gemv_kernel(AwqArgs a, i
             // codes 8u + p (low half) and 8u + p + 4 (high half): for p = 0, 2 as fp16 (1024 + q),
             // for p = 1, 3 straight from bits 4..7 as (1024 + 16 q) (exact: multiples of 16 below
             // 1024); subtracting (1024 + z), resp. (1024 + 16 z), leaves q - z, resp. 16 (q - z)
-            const __half2 zz = __float2half2_rn(1024.f + sz[i].y);
-            const __half2 zz16 = __float2half2_rn(1024.f + 16.f * sz[i].y);
-            const uint32_t cw[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
-            __half2 qz[4][4];
+            __half2 qz[2][4][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t w = cw[u], w8 = cw[u] >> 8;
-              uint32_t v0 = (w & 0x000F000Fu) | 0x64006400u, v1 = (w & 0x00F000F0u) | 0x64006400u;
-              uint32_t v2 = (w8 & 0x000F000Fu) | 0x64006400u, v3 = (w8 & 0x00F000F0u) | 0x64006400u;
-              qz[u][0] = __hsub2(*reinterpret_cast<__half2*>(&v0), zz);
-              qz[u][1] = __hsub2(*reinterpret_cast<__half2*>(&v1), zz16);
-              qz[u][2] = __hsub2(*reinterpret_cast<__half2*>(&v2), zz);
-              qz[u][3] = __hsub2(*reinterpret_cast<__half2*>(&v3), zz16);
+            for (int h = 0; h < 2; ++h) {
+              const __half2 zz = __float2half2_rn(1024.f + sz[h][i].y);
+              const __half2 zz16 = __float2half2_rn(1024.f + 16.f * sz[h][i].y);
+              const uint32_t cw[4] = {c[h][i].x, c[h][i].y, c[h][i].z, c[h][i].w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t w = cw[u], w8 = cw[u] >> 8;
+                uint32_t v0 = (w & 0x000F000Fu) | 0x64006400u, v1 = (w & 0x00F000F0u) | 0x64006400u;
+                uint32_t v2 = (w8 & 0x000F000Fu) | 0x64006400u, v3 = (w8 & 0x00F000F0u) | 0x64006400u;
+                qz[h][u][0] = __hsub2(*reinterpret_cast<__half2*>(&v0), zz);
+                qz[h][u][1] = __hsub2(*reinterpret_cast<__half2*>(&v1), zz16);
+                qz[h][u][2] = __hsub2(*reinterpret_cast<__half2*>(&v2), zz);
+                qz[h][u][3] = __hsub2(*reinterpret_cast<__half2*>(&v3), zz16);
+              }
             }
 #pragma unroll
             for (int m = 0; m < MB; ++m) {
               const uint32_t xp = ptx::smem_u32(xs_row(xs, m, K)) + uint32_t(sgi < nseg ? sgi : 0) * kSegBytes;
               // products of pairs 0, 2 and of pairs 1, 3 in two fp16 sums per two words (eight
               // products per half), then float32
-              float t = 0.f;
+              float t[2] = {0.f, 0.f};
 #pragma unroll
               for (int uu = 0; uu < 4; uu += 2) {
                 const uint4 xa = ptx::lds_v4(xp + 16u * uu), xb = ptx::lds_v4(xp + 16u * (uu + 1));
-                __half2 e = __hmul2(*reinterpret_cast<const __half2*>(&xa.x), qz[uu][0]);
-                e = __hfma2(*reinterpret_cast<const __half2*>(&xa.z), qz[uu][2], e);
-                e = __hfma2(*reinterpret_cast<const __half2*>(&xb.x), qz[uu + 1][0], e);
-                e = __hfma2(*reinterpret_cast<const __half2*>(&xb.z), qz[uu + 1][2], e);
-                __half2 o = __hmul2(*reinterpret_cast<const __half2*>(&xa.y), qz[uu][1]);
-                o = __hfma2(*reinterpret_cast<const __half2*>(&xa.w), qz[uu][3], o);
-                o = __hfma2(*reinterpret_cast<const __half2*>(&xb.y), qz[uu + 1][1], o);
-                o = __hfma2(*reinterpret_cast<const __half2*>(&xb.w), qz[uu + 1][3], o);
-                const float2 fe = __half22float2(e), fo = __half22float2(o);
-                t += (fe.x + fe.y) + (fo.x + fo.y);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  __half2 e = __hmul2(*reinterpret_cast<const __half2*>(&xa.x), qz[h][uu][0]);
+                  e = __hfma2(*reinterpret_cast<const __half2*>(&xa.z), qz[h][uu][2], e);
+                  e = __hfma2(*reinterpret_cast<const __half2*>(&xb.x), qz[h][uu + 1][0], e);
+                  e = __hfma2(*reinterpret_cast<const __half2*>(&xb.z), qz[h][uu + 1][2], e);
+                  __half2 o = __hmul2(*reinterpret_cast<const __half2*>(&xa.y), qz[h][uu][1]);
+                  o = __hfma2(*reinterpret_cast<const __half2*>(&xa.w), qz[h][uu][3], o);
+                  o = __hfma2(*reinterpret_cast<const __half2*>(&xb.y), qz[h][uu + 1][1], o);
+                  o = __hfma2(*reinterpret_cast<const __half2*>(&xb.w), qz[h][uu + 1][3], o);
+                  const float2 fe = __half22float2(e), fo = __half22float2(o);
+                  t[h] += (fe.x + fe.y) + (fo.x + fo.y);
+                }
               }
-              part[m] = fmaf(sz[i].x, t, part[m]);                 // sum x' (q - z) * sc
+#pragma unroll
+              for (int h = 0; h < 2; ++h) part[h][m] = fmaf(sz[h][i].x, t[h], part[h][m]);   // sum x' (q - z) * sc
             }
           }
         }
 #pragma unroll
-        for (int m = 0; m < MB; ++m) {
-          float v = part[m];
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && !two) break;
+          const int64_t n = n0 + h * kWarps;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-          if (lane == 0 && m0 + m < a.M) {
-            const float b = __uint_as_float(uint32_t(a.bias[n]) << 16);
-            a.Y[(m0 + m) * N + n] = uint16_t(ptx::pack_bf16x2(fmaf(v, row_up[m], b), 0.f) & 0xFFFFu);
+          for (int m = 0; m < MB; ++m) {
+            float v = part[h][m];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+            if (lane == 0 && m0 + m < a.M) {
+              const float b = __uint_as_float(uint32_t(a.bias[n]) << 16);
+              a.Y[(m0 + m) * N + n] = uint16_t(ptx::pack_bf16x2(fmaf(v, row_up[m], b), 0.f) & 0xFFFFu);
+            }
           }
         }
       }
