@@ -91,7 +91,7 @@ struct svdq_layer {
   int64_t r_pad = 0;
   // device copies
   uint8_t* d_R_codes = nullptr;
-  uint8_t* d_R_scales = nullptr;   // tiled, rows padded to 256
+  uint8_t* d_R_scales = nullptr;   // per pair tile and K step, 4 KB blocks (rows padded to 256)
   uint16_t* d_L2t = nullptr;       // N x r_pad
   unsigned char* d_LI = nullptr;   // groups of four chunks: folded + permuted L1 slices, then 1/lambda
   float* d_inv_lambda = nullptr;
@@ -412,11 +412,17 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
   // ---- device layouts on the host
   const int64_t KG = scale_groups(K);
   const int64_t Npad = round_up(N, 256);
+  // weight scales, per 256-row pair tile and 256-wide K step one contiguous 4 KB block: for each
+  // of the step's four 64-column groups, the two 128-row halves' 512-byte tiles (row r of a half
+  // at 16 (r % 32) + 4 ((r % 128) / 32), group element j % 4), so kernel 2 loads a stage's
+  // weight scales with one copy
   std::vector<uint8_t> sc_tiled(size_t(Npad / 128) * KG * 512, 0);
   for (int64_t n = 0; n < N; ++n)
-    for (int64_t j = 0; j < K / 16; ++j)
-      sc_tiled[((n / 128) * KG + j / 4) * 512 + (n % 32) * 16 + ((n % 128) / 32) * 4 + (j % 4)] =
+    for (int64_t j = 0; j < K / 16; ++j) {
+      const int64_t g = j / 4, kq = g / 4, kk = g % 4, h = (n / 128) % 2;
+      sc_tiled[(((n / 256) * (KG / 4) + kq) * 4 + kk) * 1024 + h * 512 + (n % 32) * 16 + ((n % 128) / 32) * 4 + (j % 4)] =
           hp.R_scales[n * (K / 16) + j];
+    }
   // ---- upload
   auto up = [&](void** dst, const void* src, size_t bytes) -> cudaError_t {
     cudaError_t ee;
@@ -442,7 +448,7 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
                                           : cuda_fail(e, "uploading the packed layer");
   }
   if (!encode_map_2d(h->maps.B, 1, h->d_R_codes, K / 2, N, K / 2, 128, 128, 1, &err) ||
-      !encode_map_2d(h->maps.SFB, 1, h->d_R_scales, 256, int64_t(sc_tiled.size()) / 256, 256, 256, 8, 0, &err)) {
+      !encode_map_2d(h->maps.SFB, 1, h->d_R_scales, 256, int64_t(sc_tiled.size()) / 256, 256, 256, 16, 0, &err)) {
     free_layer(h);
     delete h;
     return fail(SVDQ_ERR_CUDA, err);

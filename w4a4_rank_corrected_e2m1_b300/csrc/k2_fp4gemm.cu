@@ -295,10 +295,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const int kq = it - n_lr;
           ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
           ptx::tma_load_2d(st + A_BYTES, &maps.B, fb, 128 * kq, nb);
-          // scales: 2 KB chunks = 8 rows of the 256-byte-wide view of the tiled buffers
+          // weight scales: the pair tile's 4 KB block of this K step (16 rows of the 256-byte-wide
+          // view), both halves of each group side by side
           unsigned char* sfb = st + A_BYTES + B_BYTES + SFA_BYTES;
-          ptx::tma_load_2d(sfb, &maps.SFB, fb, 0, int(((int64_t(n0) / 128) * KG + 4 * kq) * 2));
-          ptx::tma_load_2d(sfb + SFA_BYTES, &maps.SFB, fb, 0, int(((int64_t(n0) / 128 + 1) * KG + 4 * kq) * 2));
+          ptx::tma_load_2d(sfb, &maps.SFB, fb, 0, int(((int64_t(n0) / 256) * n_k + kq) * 16));
         }
       };
       auto act_loads = [&](int it, int m0, unsigned char* st, uint64_t* fb) {
@@ -425,14 +425,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const uint32_t sfa_t = tmem + lane_off + SF_COL0 + stage * SF_COLS_PER_STAGE;
             ptx::tmem_st_32x32b_x16_rep4(sfa_t, sfa[w], sfa[128 + w], sfa[256 + w], sfa[384 + w]);
             // B scales: every lane quarter holds all 256 weight rows; column 8 kk + 4 h + j of
-            // lane i is weight row 128 h + 32 j + i, i.e. 16-byte row i of the (h, kk) tile.
+            // lane i is weight row 128 h + 32 j + i, i.e. 16-byte row i of the (kk, h) tile.
             const uint4* sfb = reinterpret_cast<const uint4*>(sfa + SFA_BYTES / 4);
             uint32_t vb[32];
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const uint4 t = sfb[h * 128 + kk * 32 + lane];
+                const uint4 t = sfb[(kk * 2 + h) * 32 + lane];
                 vb[8 * kk + 4 * h] = t.x;
                 vb[8 * kk + 4 * h + 1] = t.y;
                 vb[8 * kk + 4 * h + 2] = t.z;

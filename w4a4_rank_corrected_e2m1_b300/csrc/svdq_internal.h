@@ -115,7 +115,7 @@ struct K2Maps {
   alignas(64) unsigned char A[128];    // CUtensorMap: x codes      (u8, K/2 x M, box 128 x 128, swizzle 128)
   alignas(64) unsigned char B[128];    // CUtensorMap: R codes      (u8, K/2 x N, box 128 x 128, swizzle 128)
   alignas(64) unsigned char SFA[128];  // CUtensorMap: x scales     (u8, 256-byte rows of the tiled buffer, box 256 x 8)
-  alignas(64) unsigned char SFB[128];  // CUtensorMap: R scales     (same view)
+  alignas(64) unsigned char SFB[128];  // CUtensorMap: R scales     (same view, box 256 x 16: a pair tile's K step)
   alignas(64) unsigned char T[128];    // CUtensorMap: T            (bf16, r_pad x M, box 64 x 128, swizzle 128)
   alignas(64) unsigned char L2[128];   // CUtensorMap: L2^T         (bf16, r_pad x N, box 64 x 128, swizzle 128)
   alignas(64) unsigned char Y[128];    // CUtensorMap: Y            (bf16, N x M, box 64 x 32, swizzle 128)
