@@ -90,15 +90,14 @@ struct svdq_layer {
   int sm_count = 0;
   int64_t r_pad = 0;
   // device copies
-  uint8_t* d_R_codes = nullptr;
-  uint8_t* d_R_scales = nullptr;   // per pair tile and K step, 4 KB blocks (rows padded to 256)
+  uint8_t* d_wt = nullptr;         // kernel 2's weight blocks: codes and scales per pair tile, K step, half
   uint16_t* d_L2t = nullptr;       // N x r_pad
   unsigned char* d_LI = nullptr;   // groups of four chunks: folded + permuted L1 slices, then 1/lambda
   float* d_inv_lambda = nullptr;
   float* d_qtab = nullptr;         // activation quantiser tables (thresholds, reciprocals)
   uint16_t* d_bias = nullptr;
   int* d_err = nullptr;
-  K2Maps maps{};                   // B and L2 filled at pack
+  K2Maps maps{};                   // L2 filled at pack
   // LoRA factors appended to the low-rank branch (svdq_attach_lora): r_lora columns of
   // bf16(scale * A) after L1's columns, r_lora rows of B after L2's rows
   int64_t r_lora = 0;
@@ -158,8 +157,7 @@ svdq_status_t check_shape(int64_t N, int64_t K, int64_t r) {
 }
 
 void free_layer(svdq_layer* h) {
-  cudaFree(h->d_R_codes);
-  cudaFree(h->d_R_scales);
+  cudaFree(h->d_wt);
   cudaFree(h->d_L2t);
   cudaFree(h->d_LI);
   cudaFree(h->d_inv_lambda);
@@ -318,6 +316,7 @@ svdq_status_t launch_k2(svdq_layer* h, const void* codes, const void* scales, co
     return fail(SVDQ_ERR_CUDA, err);
   K2Args a{};
   a.bias = h->d_bias;
+  a.wt = h->d_wt;
   a.err = h->d_err;
   a.M = M;
   a.N = N;
@@ -412,17 +411,31 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
   // ---- device layouts on the host
   const int64_t KG = scale_groups(K);
   const int64_t Npad = round_up(N, 256);
-  // weight scales, per 256-row pair tile and 256-wide K step one contiguous 4 KB block: for each
-  // of the step's four 64-column groups, the two 128-row halves' 512-byte tiles (row r of a half
-  // at 16 (r % 32) + 4 ((r % 128) / 32), group element j % 4), so kernel 2 loads a stage's
-  // weight scales with one copy
-  std::vector<uint8_t> sc_tiled(size_t(Npad / 128) * KG * 512, 0);
-  for (int64_t n = 0; n < N; ++n)
+  // kernel 2's weight blocks: per 256-row pair tile, 256-wide K step and 128-row half one
+  // contiguous block, so a CTA takes a stage's weights with one bulk copy.
+  //  - codes: row r of the half, 16-byte chunk c of the step at r * 128 + 16 (c ^ (r % 8)), the
+  //    128-byte swizzle the MMA's shared-memory descriptor reads;
+  //  - then the pair tile's 4 KB scale block of the step, the same in both halves: for each of the
+  //    step's four 64-column groups, the two halves' 512-byte tiles side by side (row r of a half
+  //    at 16 (r % 32) + 4 ((r % 128) / 32), group element j % 4).
+  const int64_t n_k = KG / 4;
+  std::vector<uint8_t> wt(size_t(Npad / 128) * n_k * kK2WeightBlock, 0);
+  auto block = [&](int64_t n, int64_t kq) {
+    return wt.data() + (((n / 256) * n_k + kq) * 2 + (n / 128) % 2) * kK2WeightBlock;
+  };
+  for (int64_t n = 0; n < N; ++n) {
+    const int64_t r = n % 128;
+    for (int64_t kb = 0; kb < K / 2; kb += 16) {
+      const int64_t c = (kb % 128) / 16;
+      std::memcpy(block(n, kb / 128) + r * 128 + 16 * (c ^ (r % 8)), hp.R_codes.data() + n * (K / 2) + kb, 16);
+    }
     for (int64_t j = 0; j < K / 16; ++j) {
       const int64_t g = j / 4, kq = g / 4, kk = g % 4, h = (n / 128) % 2;
-      sc_tiled[(((n / 256) * (KG / 4) + kq) * 4 + kk) * 1024 + h * 512 + (n % 32) * 16 + ((n % 128) / 32) * 4 + (j % 4)] =
-          hp.R_scales[n * (K / 16) + j];
+      const int64_t at = 128 * 128 + kk * 1024 + h * 512 + (n % 32) * 16 + ((n % 128) / 32) * 4 + (j % 4);
+      block(n, kq)[at] = hp.R_scales[n * (K / 16) + j];   // this half's copy of the block
+      block(n ^ 128, kq)[at] = hp.R_scales[n * (K / 16) + j];   // the other half's copy
     }
+  }
   // ---- upload
   auto up = [&](void** dst, const void* src, size_t bytes) -> cudaError_t {
     cudaError_t ee;
@@ -431,8 +444,7 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
     if (bytes) ee = cudaMemcpyAsync(*dst, src, bytes, cudaMemcpyHostToDevice, stream);
     return ee;
   };
-  e = up(reinterpret_cast<void**>(&h->d_R_codes), hp.R_codes.data(), hp.R_codes.size());
-  if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_R_scales), sc_tiled.data(), sc_tiled.size());
+  e = up(reinterpret_cast<void**>(&h->d_wt), wt.data(), wt.size());
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_inv_lambda), hp.inv_lambda.data(), K * 4);
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_qtab), qtab.data(), qtab.size() * 4);
   if (e == cudaSuccess) e = up(reinterpret_cast<void**>(&h->d_bias), hp.bias.data(), N * 2);
@@ -446,12 +458,6 @@ svdq_status_t svdq_pack_weights(const svdq_pack_params_t* p, svdq_handle_t* out)
     delete h;
     return e == cudaErrorMemoryAllocation ? fail(SVDQ_ERR_OOM, "device allocation failed")
                                           : cuda_fail(e, "uploading the packed layer");
-  }
-  if (!encode_map_2d(h->maps.B, 1, h->d_R_codes, K / 2, N, K / 2, 128, 128, 1, &err) ||
-      !encode_map_2d(h->maps.SFB, 1, h->d_R_scales, 256, int64_t(sc_tiled.size()) / 256, 256, 256, 16, 0, &err)) {
-    free_layer(h);
-    delete h;
-    return fail(SVDQ_ERR_CUDA, err);
   }
   s = upload_low_rank(h, stream);
   if (s != SVDQ_OK) {
@@ -876,6 +882,7 @@ svdq_status_t mlp_up(svdq_mlp* p, const void* X, int64_t M, void* codes, void* s
     return fail(SVDQ_ERR_CUDA, err);
   K2Args a{};
   a.bias = up->d_bias;
+  a.wt = up->d_wt;
   a.err = up->d_err;
   a.M = M;
   a.N = N;

@@ -56,9 +56,13 @@ constexpr int BM = 128;                            // rows per CTA (pair tile: 2
 constexpr int BN = 256;                            // columns per pair tile
 constexpr int A_BYTES = BM * 128;                  // 128 rows x 256 fp4
 constexpr int B_BYTES = (BN / 2) * 128;            // this CTA's 128 weight rows x 256 fp4
-constexpr int SFA_BYTES = 4 * 512;                 // 4 k64-groups x (128 rows x 4 scales)
 constexpr int SFB_BYTES = 2 * 4 * 512;             // both 128-row halves of the tile's weights
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int SFA_BYTES = 4 * 512;                 // 4 k64-groups x (128 rows x 4 scales)
+// stage: A codes | B codes | B scales | A scales (B codes and scales are one weight block)
+constexpr int SFB_OFF = A_BYTES + B_BYTES;
+constexpr int SFA_OFF = SFB_OFF + SFB_BYTES;
+constexpr int STAGE_BYTES = SFA_OFF + SFA_BYTES;
+static_assert(B_BYTES + SFB_BYTES == kK2WeightBlock, "a weight block fills a stage's B codes and scales");
 constexpr int SCALE_WARP0 = 2;
 constexpr int EPI_WARP0 = 6;
 constexpr int EPI_WARPS = 8;
@@ -259,9 +263,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&maps.A);
-    ptx::prefetch_tmap(&maps.B);
     ptx::prefetch_tmap(&maps.SFA);
-    ptx::prefetch_tmap(&maps.SFB);
     if (!FUSED) ptx::prefetch_tmap(&maps.Y);
     if (n_lr) {
       ptx::prefetch_tmap(&maps.T);
@@ -294,11 +296,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         } else {
           const int kq = it - n_lr;
           ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          ptx::tma_load_2d(st + A_BYTES, &maps.B, fb, 128 * kq, nb);
-          // weight scales: the pair tile's 4 KB block of this K step (16 rows of the 256-byte-wide
-          // view), both halves of each group side by side
-          unsigned char* sfb = st + A_BYTES + B_BYTES + SFA_BYTES;
-          ptx::tma_load_2d(sfb, &maps.SFB, fb, 0, int(((int64_t(n0) / 256) * n_k + kq) * 16));
+          // this half's weight block of the step: codes already in swizzled order, then the
+          // pair tile's scales
+          const uint8_t* wb = a.wt + ((int64_t(n0 / 256) * n_k + kq) * 2 + int64_t(rank)) * kK2WeightBlock;
+          ptx::bulk_load(st + A_BYTES, wb, kK2WeightBlock, fb);
         }
       };
       auto act_loads = [&](int it, int m0, unsigned char* st, uint64_t* fb) {
@@ -307,7 +308,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         } else {
           const int kq = it - n_lr;
           ptx::tma_load_2d(st, &maps.A, fb, 128 * kq, m0);
-          ptx::tma_load_2d(st + A_BYTES + B_BYTES, &maps.SFA, fb, 0, int(((int64_t(m0) / 128) * KG + 4 * kq) * 2));
+          ptx::tma_load_2d(st + SFA_OFF, &maps.SFA, fb, 0, int(((int64_t(m0) / 128) * KG + 4 * kq) * 2));
         }
       };
       if (pre > 0) {
@@ -420,13 +421,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             // A scales: the MMA reads row 32q + lane from this lane, column base + 4 kk + q; the
             // row's four scales of k-step kk are the word at kk * 512 + lane * 16 + q * 4 of the
             // 128 x 4 tile layout (the value goes to all four columns of the group).
-            const uint32_t* sfa = reinterpret_cast<const uint32_t*>(stages + stage * STAGE_BYTES + A_BYTES + B_BYTES);
+            const uint32_t* sfa = reinterpret_cast<const uint32_t*>(stages + stage * STAGE_BYTES + SFA_OFF);
             const int w = lane * 4 + int(q);
             const uint32_t sfa_t = tmem + lane_off + SF_COL0 + stage * SF_COLS_PER_STAGE;
             ptx::tmem_st_32x32b_x16_rep4(sfa_t, sfa[w], sfa[128 + w], sfa[256 + w], sfa[384 + w]);
             // B scales: every lane quarter holds all 256 weight rows; column 8 kk + 4 h + j of
             // lane i is weight row 128 h + 32 j + i, i.e. 16-byte row i of the (kk, h) tile.
-            const uint4* sfb = reinterpret_cast<const uint4*>(sfa + SFA_BYTES / 4);
+            const uint4* sfb = reinterpret_cast<const uint4*>(stages + stage * STAGE_BYTES + SFB_OFF);
             uint32_t vb[32];
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)

@@ -113,9 +113,7 @@ int k1_launch(const K1Args& a, const K1Plan& plan, void* stream, std::string* er
 // ------------------------------------------------------------------ kernel 2 (k2_fp4gemm.cu)
 struct K2Maps {
   alignas(64) unsigned char A[128];    // CUtensorMap: x codes      (u8, K/2 x M, box 128 x 128, swizzle 128)
-  alignas(64) unsigned char B[128];    // CUtensorMap: R codes      (u8, K/2 x N, box 128 x 128, swizzle 128)
   alignas(64) unsigned char SFA[128];  // CUtensorMap: x scales     (u8, 256-byte rows of the tiled buffer, box 256 x 8)
-  alignas(64) unsigned char SFB[128];  // CUtensorMap: R scales     (same view, box 256 x 16: a pair tile's K step)
   alignas(64) unsigned char T[128];    // CUtensorMap: T            (bf16, r_pad x M, box 64 x 128, swizzle 128)
   alignas(64) unsigned char L2[128];   // CUtensorMap: L2^T         (bf16, r_pad x N, box 64 x 128, swizzle 128)
   alignas(64) unsigned char Y[128];    // CUtensorMap: Y            (bf16, N x M, box 64 x 32, swizzle 128)
@@ -132,8 +130,15 @@ struct K2Fuse {
   float* part;                // [2 S][M][rd]: partial G L1' of each unit and column half
   int rd;                     // its kernel rank (0 or a multiple of 16, <= 64)
 };
+// Weight blocks of kernel 2, one per 256-row pair tile, 256-wide K step and 128-row half, in
+// that order (K steps of a tile, then halves, innermost), kK2WeightBlock bytes each: the half's
+// 128 rows x 128 bytes of codes as a 128-byte-swizzled TMA tile would leave them in shared
+// memory (16-byte chunk c of row r at r * 128 + 16 (c ^ (r % 8))), then the pair tile's 4 KB
+// scale block of the step (both halves; see the layer's pack).
+constexpr int kK2WeightBlock = 128 * 128 + 4096;
 struct K2Args {
   const uint16_t* bias;       // N bf16
+  const uint8_t* wt;          // weight blocks (rows padded to 256, K to 256; zero padding)
   int* err;                   // device error word
   int64_t M, N, K;
   int rank;
