@@ -428,6 +428,10 @@ struct TallCfg {
   static_assert(!STACK || 3 * R + ((R + 31) / 32) * 32 <= int(TMEM_COLS), "TMEM columns");
   static_assert(!STACK || N_MMA <= 256, "MMA N");
   static_assert(!STACK || 3 * 32 * R * 4 <= STAGE_BYTES, "reduction buffer fits in one stage");
+  // K split: this CTA's share [R][32] after the reduction buffer, then rank 0's receiving slots
+  static constexpr int PART_OFF = STACK ? 3 * 32 * R : 0;          // floats from the ring's start
+  static constexpr int RECV_OFF = PART_OFF + 32 * R;
+  static_assert((RECV_OFF + kK1TallMaxSplit * 32 * R) * 4 <= STAGES * STAGE_BYTES, "split shares fit in the ring");
   static_assert(STAGES >= 3, "stages");
   static_assert(RPT == 1, "one row per thread");
 };
@@ -633,10 +637,10 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
     const int64_t row = row0 + lane;
     uint4* trow = reinterpret_cast<uint4*>(a.T + row * a.r_pad);
     // with a K split, the tile's CTAs form a cluster: each keeps its float32 share [R][32 rows]
-    // in shared memory (after the ring's reduction buffer) and cluster rank 0 adds the shares in
-    // split order through distributed shared memory
+    // in shared memory (after the ring's reduction buffer), stores it into its slot of cluster
+    // rank 0's shared memory, and rank 0 adds the slots in split order
     const bool split = tsplit > 1;
-    float* part = reinterpret_cast<float*>(ring) + 3 * 32 * R;
+    float* part = reinterpret_cast<float*>(ring) + C::PART_OFF;
     // 32 columns of T from TMEM (plus the other warps' blocks in `red`), scaled, to bf16
     auto emit = [&](int cb, const uint32_t* v, const float* red, bool ok) {
 #pragma unroll
@@ -720,39 +724,33 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
       ptx::tmem_dealloc(tmem_slot, C::TMEM_COLS);
     }
     if (split) {
-      ptx::cluster_sync();                        // every share is in its CTA's shared memory
+      // every CTA of the cluster is past its mainloop (rank 0's ring is free to receive), and
+      // every share is in its CTA's shared memory
+      ptx::cluster_sync();
+      // this split's share into slot sp of rank 0's shared memory: remote stores, made visible
+      // to rank 0 by the next barrier's release and acquire
+      float* recv = reinterpret_cast<float*>(ring) + C::RECV_OFF;
+      const uint32_t dst = ptx::mapa(ptx::smem_u32(recv + sp * 32 * R), 0u);
+      for (int e = threadIdx.x; e < 8 * R; e += blockDim.x)
+        ptx::st_cluster_v4(dst + uint32_t(e) * 16u, reinterpret_cast<const float4*>(part)[e]);
+      ptx::cluster_sync();
       if (sp == 0) {
-        // T = (sum of the shares in split order) / alpha, 32 rows x r_pad columns (zeros past R);
-        // every share is loaded before any is added
-        const uint32_t own = ptx::smem_u32(part);
+        // T = (sum of the shares in split order) / alpha, 32 rows x r_pad columns (zeros past R)
         for (int e = threadIdx.x; e < 32 * (a.r_pad / 2); e += blockDim.x) {
           const int rr = e % 32, cp = e / 32;
           uint32_t o = 0u;
           if (2 * cp < R) {
-            float p0[kK1TallMaxSplit], p1[kK1TallMaxSplit];
-            const uint32_t off0 = uint32_t(((2 * cp) * 32 + rr) * 4), off1 = off0 + 32 * 4;
-#pragma unroll
-            for (int q = 0; q < kK1TallMaxSplit; ++q) {
-              if (q < tsplit) {
-                const uint32_t base = ptx::mapa(own, uint32_t(q));
-                p0[q] = ptx::ld_cluster_f32(base + off0);
-                p1[q] = ptx::ld_cluster_f32(base + off1);
-              }
-            }
-            float s0 = p0[0], s1 = p1[0];
-#pragma unroll
-            for (int q = 1; q < kK1TallMaxSplit; ++q) {
-              if (q < tsplit) {
-                s0 += p0[q];
-                s1 += p1[q];
-              }
+            const float* s = recv + (2 * cp) * 32 + rr;
+            float s0 = s[0], s1 = s[32];
+            for (int q = 1; q < tsplit; ++q) {
+              s0 += s[q * 32 * R];
+              s1 += s[q * 32 * R + 32];
             }
             o = ptx::pack_bf16x2(s0 * a.inv_alpha, s1 * a.inv_alpha);
           }
           if (row0 + rr < M) reinterpret_cast<uint32_t*>(a.T + (row0 + rr) * a.r_pad)[cp] = o;
         }
       }
-      ptx::cluster_sync();                        // rank 0 has read every share: all may exit
     }
   }
 }

@@ -289,11 +289,10 @@ __device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t caddr) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// 32-bit load of a shared-memory word of a CTA of this cluster (address from mapa).
-__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
-  return v;
+// 16-byte store to shared memory of a CTA of this cluster (address from mapa, 16-byte aligned).
+__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
 }
 
 // 32-bit store to a shared-memory word of a CTA of this cluster (address from mapa).
