@@ -144,7 +144,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t row0 = int64_t(blockIdx.x) * kRows;
 
   ptx::griddep_launch_dependents();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) (i < 128 ? s_thr[i] : s_rcp[i - 128]) = a.qtab[i];
+  // the quantiser tables (pack-time constants) are loaded into registers here and stored after
+  // the block barrier, so that no role waits for this load before its first step: threads
+  // 0..255 all belong to quantiser warps, which meet at barrier 3 before reading the tables
+  const float qv = threadIdx.x < 256 ? __ldg(a.qtab + threadIdx.x) : 0.f;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       ptx::mbar_init(&full[i], 1);
@@ -230,6 +233,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ------------------------------------------------------------ quantiser warps
+    if (threadIdx.x < 256) (threadIdx.x < 128 ? s_thr[threadIdx.x] : s_rcp[threadIdx.x - 128]) = qv;
+    ptx::bar_sync(3, 32 * kQWarps);
     int stage = 0;
     uint32_t phase = 0;
     for (int c = c0; c < nchunks; c += nsplit) {
@@ -434,6 +439,7 @@ struct TallCfg {
   static_assert((RECV_OFF + kK1TallMaxSplit * 32 * R) * 4 <= STAGES * STAGE_BYTES, "split shares fit in the ring");
   static_assert(STAGES >= 3, "stages");
   static_assert(RPT == 1, "one row per thread");
+  static_assert(QW >= 8, "threads 0..255 (the quantiser-table loads) are quantiser threads");
 };
 
 // Stage j's L1 slices and 1/lambda parts: [CH slices][CH 1/lambda parts].
@@ -478,7 +484,10 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
   const int nsteps = s_end > s_begin ? s_end - s_begin : 0;
   const int64_t row0 = int64_t(rtile) * kTallRows;
 
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) (i < 128 ? s_thr[i] : s_rcp[i - 128]) = a.qtab[i];
+  // the quantiser tables (pack-time constants) are loaded into registers here and stored after
+  // the block barrier, so that no role waits for this load before its first step: threads
+  // 0..255 all belong to quantiser warps, which meet at barrier 3 before reading the tables
+  const float qv = threadIdx.x < 256 ? __ldg(a.qtab + threadIdx.x) : 0.f;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       ptx::mbar_init(&full[i], 1);
@@ -572,6 +581,8 @@ __global__ void __launch_bounds__(TallCfg<R>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ quantiser warps
+    if (threadIdx.x < 256) (threadIdx.x < 128 ? s_thr[threadIdx.x] : s_rcp[threadIdx.x - 128]) = qv;
+    ptx::bar_sync(3, 32 * kQWarps);
     // warp w takes chunk w / 4 of the stage and rows 8 (w % 4) .. 8 (w % 4) + 7; thread (g, t)
     // takes the 16-element block at columns 16 t .. 16 t + 15 of row 8 (w % 4) + g.  Its
     // addresses are computed once and advance by CH chunks a stage.
