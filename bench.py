@@ -43,7 +43,7 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on 
 # captures summarised under profiles/, keyed by the workload and by a hash of the kernel's
 # sources at capture time: a kernel edited since then reports null traffic.
 NCU_TRAFFIC = {
-    ("flux_mlp_up", "k1_actquant"): ("c0fad57d7bb9dac1", 28572160.0 + 0.0),
+    ("flux_mlp_up", "k1_actquant"): ("6d066dcbfff4071a", 28570624.0 + 0.0),
     ("flux_mlp_up", "k2_fp4gemm"): ("d43e44583deda194", 36343552.0 + 64710400.0),
     ("flux_mod", "awq_gemv"): ("11f7be6295e75b32", 35478016.0 + 0.0),
 }
